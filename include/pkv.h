@@ -1,0 +1,192 @@
+/*
+ * pkv.h -- C ABI of libpkv: attention for one decode step (and for a causal
+ * query chunk) over a paged BF16 KV cache, on one GB300 (sm_103a).
+ *
+ * Source of the operations. All section/figure references are to the web
+ * textbook page "Chapter 8: Inference Optimization" (clxhxhhr.top/posts/4341):
+ *   - §8.1.1 "Execution resources and request lifecycle": in decode, each step
+ *     feeds the newly generated token, reads the request's context KV and
+ *     stores the new token's K and V.
+ *   - §8.1.2 "Storage of weights, KV and runtime buffers": K and V per token
+ *     per layer are 8 KV heads x 128 dims x BF16; blocks hold 16 tokens.
+ *   - §8.3.1 "Reservation, fragmentation and paged allocation", Fig. 8-10: KV
+ *     lives in fixed-size physical blocks; a per-request block table maps
+ *     logical block j to a physical block, and attention locates each token's
+ *     KV through that table, so blocks may be scattered.
+ *   - §8.3.1 worked example and Fig. 8-13: blocks of a common prefix are
+ *     stored once and referenced from several block tables.
+ *   - §8.2.3 "Interference of long prefill with generation and chunking",
+ *     Fig. 8-8/8-9: in a chunk of c new tokens after h cached ones, new token j
+ *     (1-based) attends to h + j tokens (causal inside the chunk).
+ *   - §8.5.2: verifying several draft positions reads the same KV as one
+ *     decode step; it is the same chunked attention with a short chunk.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are caller-owned device memory; the library never allocates,
+ *     frees or synchronises, and every call only enqueues work on `stream`
+ *     (a cudaStream_t passed as void*; NULL is the legacy default stream).
+ *   - BF16 values are passed as raw 16-bit patterns (void*).
+ *   - Cache layout, per tensor (K and V are separate buffers of identical
+ *     shape):  [num_blocks][num_kv_heads][block_size][head_dim] BF16, so one
+ *     (physical block, kv head) tile of 16 x 128 BF16 = 4 KiB is contiguous.
+ *     Slot s of the pool is token (s % block_size) of physical block
+ *     (s / block_size).
+ *   - Supported shapes: block_size 16, head_dim 128, num_kv_heads >= 1,
+ *     num_q_heads = 4 * num_kv_heads (GQA groups of 4 query heads; query head
+ *     h reads KV head h / 4).  Other shapes return PKV_ERR_UNSUPPORTED.
+ *   - Argument errors detectable on the host return a non-zero status and
+ *     enqueue nothing.  Errors that depend on device data (a block id outside
+ *     the pool, a slot outside the pool, a context longer than the block
+ *     table) never fault: the kernels clamp the access into the pool and set
+ *     a device error word, read with pkv_get_device_error().
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_NULL = 1,        /* a required pointer is NULL                       */
+  PKV_ERR_SHAPE = 2,       /* a size is negative or inconsistent               */
+  PKV_ERR_UNSUPPORTED = 3, /* a shape this build has no kernel for             */
+  PKV_ERR_WORKSPACE = 4,   /* split-KV workspace missing or too small          */
+  PKV_ERR_CUDA = 5         /* a CUDA runtime call failed (launch, attribute)   */
+} pkv_status;
+
+/* Bits of the device error word (pkv_get_device_error). */
+#define PKV_DEVERR_BLOCK_ID 1u   /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_SLOT 2u       /* slot_mapping entry >= num_blocks*16       */
+#define PKV_DEVERR_CONTEXT 4u    /* context_lens[r] > max_blocks_per_seq*16   */
+#define PKV_DEVERR_TIMEOUT 8u    /* a pipeline wait gave up (never expected)  */
+
+/* Geometry of one layer's paged cache (both K and V use it). */
+typedef struct pkv_cache_desc {
+  int32_t num_blocks;   /* physical blocks in the pool                     */
+  int32_t block_size;   /* tokens per block; must be 16                    */
+  int32_t num_kv_heads; /* KV heads; query heads = 4 * num_kv_heads        */
+  int32_t head_dim;     /* must be 128                                     */
+} pkv_cache_desc;
+
+/*
+ * pkv_kv_append -- store each new token's K and V in its slot (§8.1.1: the
+ * step stores the K and V of the token it processes; §8.3.1: the slot is
+ * physical block * block_size + offset, found through the block table).
+ *
+ *   k_cache, v_cache : device, cache layout above, modified in place.
+ *   cache            : host pointer to the pool geometry.
+ *   slot_mapping     : device int64 [num_tokens]; slot of token t, or < 0 to
+ *                      skip token t (padding).  Slots must be distinct; a
+ *                      slot >= num_blocks*block_size is skipped and sets
+ *                      PKV_DEVERR_SLOT.
+ *   k_new, v_new     : device BF16 [num_tokens][num_kv_heads][head_dim].
+ *   num_tokens       : >= 0; 0 enqueues nothing and returns PKV_OK.
+ * The copy is bit-exact.
+ */
+pkv_status pkv_kv_append(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                         const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                         int32_t num_tokens, void* stream);
+
+/*
+ * pkv_choose_kv_blocks_per_split -- the split-KV heuristic used when
+ * pkv_paged_attention is given kv_blocks_per_split = 0.  Long contexts are cut
+ * into contiguous ranges of this many logical blocks, each reduced by its own
+ * CTA, so that num_seqs x num_kv_heads x splits fills the GPU's SMs.  Returns
+ * >= max_blocks_per_seq when no split is needed.  Pure host arithmetic.
+ *   sm_count : SMs of the target GPU (<= 0: ask the current CUDA device).
+ */
+int32_t pkv_choose_kv_blocks_per_split(int32_t num_seqs, int32_t num_kv_heads, int32_t q_len,
+                                       int32_t max_blocks_per_seq, int32_t sm_count);
+
+/*
+ * pkv_workspace_size -- bytes of device workspace pkv_paged_attention needs
+ * for these sizes and this (already resolved, > 0) kv_blocks_per_split; 0 when
+ * no split is made.  Layout: partial_o FP32 [num_seqs][q_len][num_q_heads]
+ * [num_splits][head_dim], then partial_lse FP32 [num_seqs][q_len][num_q_heads]
+ * [num_splits], with num_splits = ceil(max_blocks_per_seq / kv_blocks_per_split),
+ * each part 256-byte aligned.
+ */
+size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t head_dim,
+                          int32_t max_blocks_per_seq, int32_t kv_blocks_per_split);
+
+/*
+ * pkv_paged_attention -- softmax(q K^T * scale) V for every request, query
+ * position and query head, reading K/V through the block tables.
+ *
+ *   out          : device BF16 [num_seqs][q_len][num_q_heads][head_dim].
+ *   q            : device BF16, same shape as out.
+ *   k_cache, v_cache, cache : as for pkv_kv_append (read only).
+ *   block_tables : device int32 [num_seqs][max_blocks_per_seq]; entry j of row
+ *                  r is the physical block holding logical block j of request
+ *                  r (tokens 16j .. 16j+15).  Rows may share entries (common
+ *                  prefixes).  Entries past ceil(ctx/16) are never read.
+ *   context_lens : device int32 [num_seqs]; ctx_r = number of tokens of
+ *                  request r in the cache, INCLUDING the q_len tokens of this
+ *                  step (append first, then attend).  Query i (0-based) of
+ *                  request r sits at position ctx_r - q_len + i and attends to
+ *                  the keys at positions 0 .. ctx_r - q_len + i.  ctx_r = 0 is a
+ *                  padding row: its outputs are zero.  A query with no visible
+ *                  key (ctx_r < q_len) also outputs zeros.
+ *   q_len        : query tokens per request (1 = plain decode; >= 2 = causal
+ *                  chunk).  q_len >= 16 runs on the tensor-core kernel.
+ *   num_q_heads  : 4 * cache->num_kv_heads.
+ *   scale        : logit scale (1/sqrt(head_dim) for standard attention).
+ *   kv_blocks_per_split : 0 = choose with pkv_choose_kv_blocks_per_split;
+ *                  >= max_blocks_per_seq = one pass per (request, kv head);
+ *                  otherwise each request's blocks are reduced in ranges of
+ *                  this many blocks and merged by the combine kernel.
+ *   workspace, workspace_bytes : device scratch of at least
+ *                  pkv_workspace_size(...) bytes for the resolved split (may be
+ *                  NULL/0 when no split is made).  Its contents are
+ *                  overwritten; calls that share it must be stream-ordered.
+ * The result does not depend on where blocks sit in the pool; with a fixed
+ * split it is bitwise reproducible.  The split changes rounding only.
+ */
+pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const pkv_cache_desc* cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t num_seqs, int32_t q_len, int32_t num_q_heads, float scale,
+                               int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * pkv_attn_combine -- merge split-KV partial results (the log-sum-exp
+ * identity of blockwise softmax: a softmax over the union of key ranges is
+ * the lse-weighted mix of the per-range softmaxes).
+ *
+ *   out         : device BF16 [num_rows][head_dim], num_rows = num_seqs*q_len*
+ *                 num_q_heads.
+ *   partial_o   : device FP32 [num_rows][num_splits][head_dim]; split s holds
+ *                 its own normalised softmax(q K_s^T) V_s.
+ *   partial_lse : device FP32 [num_rows][num_splits]; natural-log
+ *                 log-sum-exp of split s's scaled logits, -inf for an empty
+ *                 split (its partial_o is then ignored).
+ *   out_lse     : optional device FP32 [num_rows] (NULL to skip): the merged
+ *                 log-sum-exp.
+ * out = sum_s exp(lse_s - lse) * O_s with lse = log sum_s exp(lse_s); a row
+ * whose splits are all empty gets zeros (and out_lse = -inf).
+ */
+pkv_status pkv_attn_combine(void* out, float* out_lse, const float* partial_o,
+                            const float* partial_lse, int32_t num_rows, int32_t head_dim,
+                            int32_t num_splits, void* stream);
+
+/*
+ * pkv_get_device_error -- copy the device error word (PKV_DEVERR_* bits,
+ * accumulated over all calls on the current device since the last reset) to
+ * *host_word; when reset != 0, clear it.  Synchronises the device.
+ */
+pkv_status pkv_get_device_error(uint32_t* host_word, int32_t reset);
+
+/* Human-readable name of a status code (static string). */
+const char* pkv_status_string(pkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

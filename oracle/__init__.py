@@ -1,0 +1,162 @@
+"""FP64 CPU oracle for paged KV decode attention -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+and reference legs may import this package.  The library never does, and this
+package imports nothing from the library: the two share only the seeded input
+generator (``workloads``).
+
+Contents:
+  * ``pkv_oracle.c`` (built here into ``_build/liboracle.so``): the plain
+    definition in C, FP64, OpenMP over output rows;
+  * ``brute``: an independent dense NumPy restatement for tiny inputs;
+  * ``sizes``: the pages' sizing arithmetic (bytes per token, blocks, waste,
+    capacity), pinned by the printed values in the tests.
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (OpenMP) into oracle/_build/liboracle.so."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    c_p = ctypes.c_void_p
+    i32 = ctypes.c_int32
+    lib.oracle_kv_append.argtypes = [c_p, c_p, i32, i32, i32, i32, c_p, c_p, c_p, i32]
+    lib.oracle_kv_append.restype = None
+    lib.oracle_visible_pairs.argtypes = [c_p, i32, i32]
+    lib.oracle_visible_pairs.restype = ctypes.c_int64
+    lib.oracle_paged_attention.argtypes = [c_p, c_p, c_p, c_p, c_p, i32, i32, i32, i32, c_p, i32,
+                                           c_p, i32, i32, i32, ctypes.c_double, c_p, i32, i32]
+    lib.oracle_paged_attention.restype = ctypes.c_int
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = i32
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+@contextlib.contextmanager
+def swapped_library(path: str):
+    """Run the Python entry points against another build of pkv_oracle.c
+    (used by the tests that plant mistakes in the oracle to prove the pins
+    catch them)."""
+    global _lib
+    saved = _load()
+    _lib = _bind(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        _lib = saved
+
+
+def build_variant(source_text: str, out_path: str) -> str:
+    """Compile an edited copy of pkv_oracle.c (test use only)."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", src, "-o", out_path, "-lm"],
+                   check=True)
+    return out_path
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def kv_append(k_cache: np.ndarray, v_cache: np.ndarray, slot_mapping: np.ndarray,
+              k_new: np.ndarray, v_new: np.ndarray) -> None:
+    """In place: store new K/V rows in their slots (uint16 BF16 bit patterns)."""
+    lib = _load()
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous
+    assert v_cache.dtype == np.uint16 and v_cache.flags.c_contiguous
+    nb, hkv, bs, d = k_cache.shape
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    t = slot_mapping.shape[0]
+    assert k_new.shape == (t, hkv, d) and v_new.shape == (t, hkv, d)
+    lib.oracle_kv_append(_ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d, _ptr(slot_mapping),
+                         _ptr(k_new), _ptr(v_new), t)
+
+
+def visible_pairs(context_lens, q_len: int) -> int:
+    """(query, key) pairs admitted by the oracle's causal rule."""
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    return int(_load().oracle_visible_pairs(_ptr(ctx), ctx.shape[0], q_len))
+
+
+def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                    block_tables: np.ndarray, context_lens: np.ndarray, q_len: int, scale: float,
+                    seq_ids=None, num_threads: int = 0, with_lse: bool = False):
+    """FP64 attention for every (selected) request; returns float64
+    [n_sel][q_len][Hq][D] (and the natural-log lse [n_sel][q_len][Hq])."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint16)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint16)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    b, ql, hq, d = q.shape
+    assert ql == q_len
+    nb, hkv, bs, d2 = k_cache.shape
+    assert d2 == d and v_cache.shape == k_cache.shape and hq % hkv == 0
+    ids = None
+    n_sel = b
+    if seq_ids is not None:
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        n_sel = ids.shape[0]
+    out = np.zeros((n_sel, q_len, hq, d), dtype=np.float64)
+    lse = np.zeros((n_sel, q_len, hq), dtype=np.float64)
+    rc = lib.oracle_paged_attention(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    nb, bs, hkv, d, _ptr(tables), tables.shape[1], _ptr(ctx), b,
+                                    q_len, hq, float(scale), _ptr(ids),
+                                    0 if ids is None else n_sel, int(num_threads))
+    if rc != 0:
+        raise ValueError("block table entry outside the pool")
+    return (out, lse) if with_lse else out
+
+
+def run_workload(w, seq_ids=None, num_threads: int = 0, with_lse: bool = False, append: bool = True):
+    """Apply the step's kv_append to copies of the pools, then attend."""
+    kc = w.k_cache.copy()
+    vc = w.v_cache.copy()
+    if append:
+        kv_append(kc, vc, w.slot_mapping, w.k_new, w.v_new)
+    return paged_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.q_len, w.scale,
+                           seq_ids=seq_ids, num_threads=num_threads, with_lse=with_lse)

@@ -1,0 +1,174 @@
+/*
+ * pkv_oracle.c -- TEST INFRASTRUCTURE, not part of the library.
+ *
+ * A plain, slow, FP64 CPU statement of what paged KV decode attention
+ * computes.  It exists only to check the CUDA path: nothing in the library
+ * links, imports or calls it.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline / reference leg may load it.  It shares no code
+ * with the CUDA path.
+ *
+ * What it follows, on the web textbook page "Chapter 8: Inference
+ * Optimization" (clxhxhhr.top/posts/4341):
+ *   - §8.1.1: in a decode step the model feeds the new token, reads the
+ *     request's context KV and stores the new token's K and V;
+ *   - §8.3.1 and Fig. 8-10: KV lives in fixed-size physical blocks; the
+ *     request's block table maps logical block j (tokens j*p .. j*p+p-1) to a
+ *     physical block, and attention finds each token's KV through it;
+ *   - §8.3.1 worked example, Fig. 8-13: several block tables may reference
+ *     the same physical block (a common prefix stored once);
+ *   - §8.2.3, Fig. 8-8/8-9: of c new tokens after h cached ones, new token j
+ *     (1-based) attends to the first h + j tokens.
+ * The attention itself is the textbook definition out = softmax(scale*q.K^T) V
+ * over the visible keys, evaluated directly in double precision: every logit,
+ * then the maximum, then exp(s - max), their sum, and the weighted sum of V.
+ * No blocking, no online rescaling, no reordering.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* BF16 is the upper half of an IEEE binary32. */
+static double bf16_value(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Index of element d of token `off` of KV head `kvh` in physical block `blk`,
+ * for the pool layout [num_blocks][num_kv_heads][block_size][head_dim]. */
+static int64_t cache_index(int64_t blk, int32_t kvh, int32_t off, int32_t d, int32_t num_kv_heads,
+                           int32_t block_size, int32_t head_dim) {
+  return ((blk * num_kv_heads + kvh) * block_size + off) * (int64_t)head_dim + d;
+}
+
+/* Query i (0-based) of a request whose cache holds ctx tokens, q_len of them
+ * new this step, sits at position ctx - q_len + i and sees key positions
+ * 0 .. ctx - q_len + i (causal within the chunk; plain decode when q_len=1). */
+static int key_visible(int64_t t, int32_t ctx, int32_t q_len, int32_t i) {
+  return t < ctx && t <= (int64_t)ctx - q_len + i;
+}
+
+/* Store each new token's K and V in its slot: physical block slot / p,
+ * offset slot % p.  Negative slots are padding and skipped; so are slots past
+ * the pool. */
+void oracle_kv_append(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks, int32_t block_size,
+                      int32_t num_kv_heads, int32_t head_dim, const int64_t* slot_mapping,
+                      const uint16_t* k_new, const uint16_t* v_new, int32_t num_tokens) {
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= (int64_t)num_blocks * block_size) continue;
+    int64_t blk = slot / block_size;
+    int32_t off = (int32_t)(slot % block_size);
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      for (int32_t d = 0; d < head_dim; ++d) {
+        int64_t dst = cache_index(blk, h, off, d, num_kv_heads, block_size, head_dim);
+        int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim + d;
+        k_cache[dst] = k_new[src];
+        v_cache[dst] = v_new[src];
+      }
+    }
+  }
+}
+
+/* Number of (query, key) pairs the causal rule admits over a batch. */
+int64_t oracle_visible_pairs(const int32_t* context_lens, int32_t num_seqs, int32_t q_len) {
+  int64_t n = 0;
+  for (int32_t r = 0; r < num_seqs; ++r)
+    for (int32_t i = 0; i < q_len; ++i)
+      for (int64_t t = 0; t < context_lens[r]; ++t) n += key_visible(t, context_lens[r], q_len, i);
+  return n;
+}
+
+/*
+ * out     : [n_sel][q_len][num_q_heads][head_dim] doubles, n_sel = num_ids when
+ *           seq_ids != NULL (rows seq_ids[0..num_ids)), else num_seqs.
+ * out_lse : same rows without head_dim (natural log); may be NULL.
+ * A query with no visible key gets zeros and lse = -inf.
+ * Returns 0, or -1 when a table entry that must be read lies outside the pool.
+ */
+int oracle_paged_attention(double* out, double* out_lse, const uint16_t* q, const uint16_t* k_cache,
+                           const uint16_t* v_cache, int32_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                           int32_t q_len, int32_t num_q_heads, double scale, const int32_t* seq_ids,
+                           int32_t num_ids, int32_t num_threads) {
+  int32_t n_sel = seq_ids ? num_ids : num_seqs;
+  int32_t group = num_q_heads / num_kv_heads; /* query heads per KV head */
+  int64_t n_rows = (int64_t)n_sel * q_len * num_q_heads;
+  int bad = 0;
+
+  for (int32_t s = 0; s < n_sel; ++s) {
+    int32_t r = seq_ids ? seq_ids[s] : s;
+    int32_t ctx = context_lens[r];
+    for (int64_t j = 0; j * block_size < ctx && !bad; ++j) {
+      if (j >= max_blocks_per_seq) {
+        bad = 1;
+        break;
+      }
+      int32_t blk = block_tables[(int64_t)r * max_blocks_per_seq + j];
+      if (blk < 0 || blk >= num_blocks) bad = 1;
+    }
+  }
+  if (bad) return -1;
+
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t row = 0; row < n_rows; ++row) {
+    int32_t h = (int32_t)(row % num_q_heads);
+    int32_t i = (int32_t)((row / num_q_heads) % q_len);
+    int32_t s = (int32_t)(row / ((int64_t)num_q_heads * q_len));
+    int32_t r = seq_ids ? seq_ids[s] : s;
+    int32_t ctx = context_lens[r];
+    int32_t kvh = h / group;
+    const uint16_t* qv = q + (((int64_t)r * q_len + i) * num_q_heads + h) * head_dim;
+    double* o = out + row * head_dim;
+    for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+
+    double* logit = (double*)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+    double m = -INFINITY;
+    for (int64_t t = 0; t < ctx; ++t) {
+      if (!key_visible(t, ctx, q_len, i)) continue;
+      int64_t blk = block_tables[(int64_t)r * max_blocks_per_seq + t / block_size];
+      int32_t off = (int32_t)(t % block_size);
+      double dot = 0.0;
+      for (int32_t d = 0; d < head_dim; ++d)
+        dot += bf16_value(qv[d]) *
+               bf16_value(k_cache[cache_index(blk, kvh, off, d, num_kv_heads, block_size, head_dim)]);
+      logit[t] = scale * dot;
+      if (logit[t] > m) m = logit[t];
+    }
+    double denom = 0.0;
+    for (int64_t t = 0; t < ctx; ++t) {
+      if (!key_visible(t, ctx, q_len, i)) continue;
+      denom += exp(logit[t] - m);
+    }
+    for (int64_t t = 0; t < ctx; ++t) {
+      if (!key_visible(t, ctx, q_len, i)) continue;
+      int64_t blk = block_tables[(int64_t)r * max_blocks_per_seq + t / block_size];
+      int32_t off = (int32_t)(t % block_size);
+      double w = exp(logit[t] - m) / denom;
+      for (int32_t d = 0; d < head_dim; ++d)
+        o[d] += w * bf16_value(
+                        v_cache[cache_index(blk, kvh, off, d, num_kv_heads, block_size, head_dim)]);
+    }
+    if (out_lse) out_lse[row] = denom > 0.0 ? m + log(denom) : -INFINITY;
+    free(logit);
+  }
+  return 0;
+}
+
+/* Threads the OpenMP runtime would use (1 without OpenMP). */
+int32_t oracle_max_threads(void) {
+#ifdef _OPENMP
+  return (int32_t)omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
