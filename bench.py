@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Benchmark of paged KV decode attention on GB300.
+
+One step = one decode step of the attention part of a 36-layer model: for
+every layer, kv_append of the batch's new tokens, then paged_attention over
+the whole batch (split-KV + combine when the library's heuristic splits).
+Every layer has its own KV pool, so consecutive layer-calls never find their
+KV in L2 (the 36 pools together are far larger than the 129 MB L2).
+
+Prints ONE JSON line (rank 0).  `value` is achieved HBM throughput in GB/s on
+the algorithmic bytes: the unique physical KV slots read (a shared-prefix
+block counts once), Q and output, the block-table entries and context
+lengths read, plus the append's read and write of the new tokens' K/V.
+
+  python bench.py [--workload short|long|mixed|chunk|tiny] [--steps K] [--warmup W]
+                  [--kv-blocks-per-split S] [--graph] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention µs/layer & achieved HBM GB/s (% of GB300 peak), 1 GPU"
+KV_BYTES_PER_TOKEN = 2 * W.NUM_KV_HEADS * W.HEAD_DIM * 2  # K and V of one token in one layer
+
+
+# ---------------------------------------------------------------------------
+# workload selection
+# ---------------------------------------------------------------------------
+
+def make_workload(name: str, seed: int):
+    if name == "short":
+        return W.short_chat(seed=seed, fill_cache=False), W.NUM_LAYERS
+    if name == "long":
+        return W.long_shared(seed=seed, fill_cache=False), W.NUM_LAYERS
+    if name == "mixed":
+        return W.mixed(seed=seed, fill_cache=False), W.NUM_LAYERS
+    if name == "chunk":
+        return W.chunk(seed=seed, fill_cache=False), 1
+    if name == "tiny":
+        return W.tiny(seed=seed, fill_cache=False), W.NUM_LAYERS
+    raise SystemExit(f"unknown workload {name}")
+
+
+WORKLOAD_TEXT = {
+    "short": "short-chat decode: 37 requests x (2048 + U{0..255}) tokens, 36 layers, 12 GiB pool",
+    "long": "long-context decode: 16 requests x (8192 + U{0..255}) tokens, 6144-token shared prefix, 36 layers",
+    "mixed": "mixed batch: 48 short + 16 long (shared prefix) + 8 requests of 1..15 tokens, 36 layers",
+    "chunk": "streaming chunks: 128 requests, q_len 16 causal, history logU[1K,32K], 1 layer (4.8 GB)",
+    "tiny": "tiny: 4 requests, contexts {17,64,100,256}, 36 layers",
+}
+
+
+def bytes_per_layer(w):
+    """(attention algorithmic bytes, append bytes) of one layer-call."""
+    uniq = w.unique_tokens()
+    qo = 2 * w.num_seqs * w.q_len * w.num_q_heads * w.head_dim * 2
+    table = sum(-(-int(c) // 16) for c in w.context_lens) * 4 + w.num_seqs * 4
+    attn = uniq * KV_BYTES_PER_TOKEN + qo + table
+    t = int((w.slot_mapping >= 0).sum())
+    append = t * KV_BYTES_PER_TOKEN * 2 + w.slot_mapping.size * 8  # read new K/V, write slots, read slot ids
+    return attn, append
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv") if os.path.isdir(
+            os.path.join(ROOT, "gpurun_out")) else f"/tmp/pkv_clocks_{os.getpid()}.csv"
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no collective on the data path)
+# ---------------------------------------------------------------------------
+
+def dist_init(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reported baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, kc_dev, vc_dev, max_seqs: int):
+    """Host copies of the blocks `max_seqs` requests read (layer 0), tables remapped."""
+    seq_ids = list(range(min(max_seqs, w.num_seqs)))
+    need = {}
+    for r in seq_ids:
+        for b in w.block_tables[r, :-(-int(w.context_lens[r]) // 16)]:
+            need.setdefault(int(b), len(need))
+    ids = torch.tensor(sorted(need, key=need.get), dtype=torch.long, device=kc_dev.device)
+    kc = kc_dev.index_select(0, ids).cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    vc = vc_dev.index_select(0, ids).cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    tables = np.vectorize(lambda b: need.get(int(b), 0))(w.block_tables[seq_ids]).astype(np.int32)
+    sl = w.slot_mapping.reshape(w.num_seqs, w.q_len)[seq_ids].reshape(-1)
+    sl = np.array([need[int(s) // 16] * 16 + int(s) % 16 if s >= 0 else -1 for s in sl], np.int64)
+    sub = W.Workload(**{**w.__dict__, "k_cache": kc, "v_cache": vc, "block_tables": tables,
+                        "context_lens": w.context_lens[seq_ids].copy(), "q": w.q[seq_ids].copy(),
+                        "k_new": w.k_new.reshape(w.num_seqs, w.q_len, -1, 128)[seq_ids].reshape(-1, w.num_kv_heads, 128),
+                        "v_new": w.v_new.reshape(w.num_seqs, w.q_len, -1, 128)[seq_ids].reshape(-1, w.num_kv_heads, 128),
+                        "slot_mapping": sl})
+    return sub
+
+
+def time_oracle(sub, budget_s: float = 12.0, max_reps: int = 200):
+    """Run the oracle's append + attention on the sample until ~budget_s; GB/s of algorithmic bytes."""
+    import oracle
+    attn_b, app_b = bytes_per_layer(sub)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.kv_append(sub.k_cache, sub.v_cache, sub.slot_mapping, sub.k_new, sub.v_new)
+        oracle.paged_attention(sub.q, sub.k_cache, sub.v_cache, sub.block_tables, sub.context_lens, sub.q_len,
+                               sub.scale)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    per = el / reps
+    return {"gbs": (attn_b + app_b) / per / 1e9, "s_per_layer_call": per, "reps": reps,
+            "cores": oracle.max_threads(), "seqs": sub.num_seqs}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="short", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--kv-blocks-per-split", type=int, default=0)
+    ap.add_argument("--graph", action="store_true", help="replay each step as one CUDA graph")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--oracle-budget-s", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_init(args.gpus)
+    w, layers = make_workload(args.workload, args.seed)
+    attn_b, app_b = bytes_per_layer(w)
+    step_bytes = layers * (attn_b + app_b)
+    tokens_layers = int(w.context_lens.sum()) * w.q_len * layers if w.q_len > 1 else int(w.context_lens.sum()) * layers
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank, w, layers, step_bytes)
+
+    import paged_kv_decode_attention_gb300 as pkv
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = pkv.lib()
+    b, ql, hq, hkv, d = w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim
+    maxb = w.max_blocks_per_seq
+    bps = args.kv_blocks_per_split or pkv.choose_kv_blocks_per_split(b, hkv, ql, maxb)
+    bps = min(bps, maxb)
+    splits = -(-maxb // bps)
+
+    # device state: per-layer pools (filled on the device), per-layer step inputs/outputs
+    pool_shape = (layers, w.num_blocks, hkv, 16, d)
+    k_pool = torch.empty(pool_shape, dtype=torch.bfloat16, device=dev)
+    v_pool = torch.empty(pool_shape, dtype=torch.bfloat16, device=dev)
+    for l in range(layers):
+        W.fill_pool_device(k_pool[l], 1000 + 2 * l + args.seed * 7919)
+        W.fill_pool_device(v_pool[l], 1001 + 2 * l + args.seed * 7919)
+    rng = np.random.Generator(np.random.PCG64(args.seed + 17))
+    t_tok = w.slot_mapping.size
+    h_q = torch.from_numpy(W.randn_bf16(rng, (layers, b, ql, hq, d))).view(torch.bfloat16)
+    h_kn = torch.from_numpy(W.randn_bf16(rng, (layers, t_tok, hkv, d))).view(torch.bfloat16)
+    h_vn = torch.from_numpy(W.randn_bf16(rng, (layers, t_tok, hkv, d))).view(torch.bfloat16)
+    h_q[0] = torch.from_numpy(w.q).view(torch.bfloat16)
+    h_kn[0] = torch.from_numpy(w.k_new).view(torch.bfloat16)
+    h_vn[0] = torch.from_numpy(w.v_new).view(torch.bfloat16)
+    h_tables = torch.from_numpy(w.block_tables)
+    h_ctx = torch.from_numpy(w.context_lens)
+    h_slots = torch.from_numpy(w.slot_mapping)
+    q = h_q.to(dev)
+    kn, vn = h_kn.to(dev), h_vn.to(dev)
+    tables, ctx, slots = h_tables.to(dev), h_ctx.to(dev), h_slots.to(dev)
+    out = torch.empty_like(q)
+    ws_bytes = pkv.workspace_size(b, ql, hq, maxb, bps)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    desc = pkv.CacheDesc(w.num_blocks, 16, hkv, d)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    pool_stride = w.num_blocks * hkv * 16 * d * 2
+    kp0, vp0 = k_pool.data_ptr(), v_pool.data_ptr()
+    q_stride, kn_stride = b * ql * hq * d * 2, t_tok * hkv * d * 2
+    launches_per_layer = 1 + 1 + (1 if splits > 1 else 0)
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {lib.pkv_status_string(st).decode()}")
+
+    def layer_call(l, ev=None):
+        check(lib.pkv_kv_append(kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc), slots.data_ptr(),
+                                kn.data_ptr() + l * kn_stride, vn.data_ptr() + l * kn_stride, t_tok, sp),
+              "kv_append")
+        if ev is not None:
+            ev[0].record(stream)
+        check(lib.pkv_paged_attention(out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride,
+                                      kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc),
+                                      tables.data_ptr(), maxb, ctx.data_ptr(), b, ql, hq, w.scale, bps,
+                                      ws.data_ptr(), ws.numel(), sp), "paged_attention")
+        if ev is not None:
+            ev[1].record(stream)
+
+    def step(events=None):
+        for l in range(layers):
+            layer_call(l, None if events is None else events[l])
+
+    graph = None
+    if args.graph:
+        step()  # warm the library's per-device lookups before capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        run_step = lambda events=None: graph.replay()
+    else:
+        run_step = step
+
+    for _ in range(args.warmup):
+        run_step()
+    torch.cuda.synchronize()
+    if pkv.get_device_error(reset=True) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- timed region (device events on the launching stream) ----
+    attn_events = None if graph is not None else [[(torch.cuda.Event(enable_timing=True),
+                                                    torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
+                                                  for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        run_step(None if attn_events is None else attn_events[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms_total = all_max(t_start.elapsed_time(t_end), world)
+    ms_per_step = ms_total / args.steps
+    if attn_events is not None:
+        attn_ms = [e[0].elapsed_time(e[1]) for st in attn_events for e in st]
+        attn_us = statistics.mean(attn_ms) * 1e3
+    else:
+        attn_us = ms_per_step * 1e3 / layers  # graph replay: whole layer-call incl. append
+    if pkv.get_device_error(reset=True) != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        p_q, p_kn, p_vn = h_q.pin_memory(), h_kn.pin_memory(), h_vn.pin_memory()
+        p_tables, p_ctx, p_slots = h_tables.pin_memory(), h_ctx.pin_memory(), h_slots.pin_memory()
+        p_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (p_q, p_kn, p_vn, p_tables, p_ctx, p_slots))
+        d2h = p_out.numel() * p_out.element_size()
+
+        def e2e_step():
+            for dst, src in ((q, p_q), (kn, p_kn), (vn, p_vn), (tables, p_tables), (ctx, p_ctx), (slots, p_slots)):
+                dst.copy_(src, non_blocking=True)
+            for l in range(layers):
+                pkv.kv_append(k_pool[l], v_pool[l], slots, kn[l], vn[l])
+                pkv.paged_attention(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, ql, w.scale,
+                                    kv_blocks_per_split=bps, workspace=ws)
+            p_out.copy_(out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        el = all_max(time.perf_counter() - t0, world)
+        e2e = {"value": round(world * step_bytes / (el / args.steps) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(el / args.steps * 1e3, 4), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    # ---- CPU oracle baseline (rank 0 at N=1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sub = oracle_sample(w, k_pool[0], v_pool[0], max_seqs=w.num_seqs)
+        r = time_oracle(sub, budget_s=args.oracle_budget_s)
+        cpu = {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+               "sample": f"layer 0 of this workload ({r['seqs']} requests, append + attention), FP64 C oracle, "
+                         f"{r['reps']} repetitions, {r['s_per_layer_call'] * 1e3:.1f} ms per layer-call"}
+
+    if rank != 0:
+        return
+    peaks = {}
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        peaks = json.load(open(pp))
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured"
+    if not peak:
+        peak, peak_src = 6800.0, "fallback"
+    achieved = attn_b / (attn_us * 1e-6) / 1e9
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath)).get(args.workload)
+        if tj and tj.get("kernel_build") == kernel_build_id():
+            traffic = tj.get("bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_seqs": b, "q_len": ql,
+                   "layers": layers, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16,
+                   "ctx_min": int(w.context_lens.min()), "ctx_max": int(w.context_lens.max()),
+                   "kv_blocks_per_split": bps, "splits": splits, "cuda_graph": bool(graph is not None),
+                   "l2": "inputs larger than L2: one KV pool per layer, %.1f GB total" % (
+                       2 * k_pool.numel() * 2 / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "us_per_layer_call": round(attn_us, 3),
+        "attention_tokens_layers_per_s": round(world * tokens_layers / (ms_per_step * 1e-3), 1),
+        "decode_steps_per_s": round(1e3 / ms_per_step, 2),
+        "bytes_per_step": int(step_bytes),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
+                     "kernel": "paged_attention call (decode%s)" % (" + combine" if splits > 1 else ""),
+                     "algorithmic_bytes_per_launch": int(attn_b)},
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(launches_per_layer * layers * args.steps),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def kernel_build_id() -> str:
+    """Hash of the CUDA sources: traffic numbers are valid only for the build they were taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_attention_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        h.update(fn.encode())
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def run_reference(args, world, rank, w, layers, step_bytes):
+    """Reference arm: the FP64 CPU oracle, as it stands, on the host cores;
+    each step is a bounded sample (some requests of one layer) of the workload."""
+    if rank != 0:
+        return
+    import oracle
+    # build a host pool for a bounded sample of requests
+    max_seqs = max(1, min(w.num_seqs, 8))
+    sub = W.build("sample", w.context_lens[:max_seqs], int(sum(-(-int(c) // 16) for c in w.context_lens[:max_seqs])) + 8,
+                  q_len=w.q_len, seed=args.seed)
+    attn_b, app_b = bytes_per_layer(sub)
+    for _ in range(args.warmup):
+        oracle.kv_append(sub.k_cache, sub.v_cache, sub.slot_mapping, sub.k_new, sub.v_new)
+        oracle.paged_attention(sub.q, sub.k_cache, sub.v_cache, sub.block_tables, sub.context_lens, sub.q_len,
+                               sub.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.kv_append(sub.k_cache, sub.v_cache, sub.slot_mapping, sub.k_new, sub.v_new)
+        oracle.paged_attention(sub.q, sub.k_cache, sub.v_cache, sub.block_tables, sub.context_lens, sub.q_len,
+                               sub.scale)
+    el = (time.perf_counter() - t0) / args.steps
+    value = (attn_b + app_b) / el / 1e9
+    sample = (f"{max_seqs} of {w.num_seqs} requests of one layer of the {args.workload} workload "
+              f"(append + attention) per step, FP64 C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
+                             "cores": oracle.max_threads(), "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -17,13 +17,14 @@ from __future__ import annotations
 import contextlib
 import ctypes
 import os
+import platform
 import subprocess
 
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pkv_oracle.c")
-_BUILD = os.path.join(_HERE, "_build")
+_BUILD = os.path.join(_HERE, "_build", platform.machine())
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lib = None
 
@@ -160,3 +161,30 @@ def run_workload(w, seq_ids=None, num_threads: int = 0, with_lse: bool = False, 
         kv_append(kc, vc, w.slot_mapping, w.k_new, w.v_new)
     return paged_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.q_len, w.scale,
                            seq_ids=seq_ids, num_threads=num_threads, with_lse=with_lse)
+
+
+def attn_combine(partial_o: np.ndarray, partial_lse: np.ndarray):
+    """Merge per-range attention results, FP64.
+
+    partial_o [rows][S][D] holds each key range's own normalised softmax
+    output and partial_lse [rows][S] its natural-log log-sum-exp (-inf for a
+    range without keys).  A softmax over the union of disjoint ranges is the
+    mix of the per-range ones weighted by exp(lse_s - lse), lse = log sum_s
+    exp(lse_s).  Returns (out [rows][D], lse [rows]); rows without keys give
+    zeros and -inf.
+    """
+    po = np.asarray(partial_o, dtype=np.float64)
+    pl = np.asarray(partial_lse, dtype=np.float64)
+    rows, s, d = po.shape
+    out = np.zeros((rows, d))
+    lse = np.full(rows, -np.inf)
+    for r in range(rows):
+        finite = np.isfinite(pl[r])
+        if not finite.any():
+            continue
+        m = pl[r][finite].max()
+        total = np.log(np.exp(pl[r][finite] - m).sum()) + m
+        w = np.exp(pl[r][finite] - total)
+        out[r] = (w[:, None] * po[r][finite]).sum(axis=0)
+        lse[r] = total
+    return out, lse

@@ -1,0 +1,201 @@
+"""paged_kv_decode_attention_gb300 -- Python binding of libpkv (C ABI in include/pkv.h).
+
+Argument marshalling only: each function checks tensor dtypes/devices/shapes,
+passes raw device pointers and the current CUDA stream to the exported C
+function of the same name, and turns a non-zero status into PkvError.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU
+or PyTorch fallback, and importing this module fails loudly when the shared
+library cannot be built or loaded.
+
+PyTorch provides device memory and streams only.  BF16 tensors are passed as
+torch.bfloat16 (or int16/uint16 holding BF16 bit patterns).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "PkvError", "kv_append", "paged_attention", "attn_combine", "workspace_size",
+    "choose_kv_blocks_per_split", "get_device_error", "library_path", "lib", "DEVERR_BLOCK_ID",
+    "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT",
+]
+
+DEVERR_BLOCK_ID = 1
+DEVERR_SLOT = 2
+DEVERR_CONTEXT = 4
+DEVERR_TIMEOUT = 8
+
+BLOCK_SIZE = 16
+HEAD_DIM = 128
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.pkv_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg}")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+def _load():
+    path = _build.build()
+    lib = ctypes.CDLL(path)
+    p, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    lib.pkv_kv_append.argtypes = [p, p, ctypes.POINTER(CacheDesc), p, p, p, i32, p]
+    lib.pkv_kv_append.restype = ctypes.c_int
+    lib.pkv_choose_kv_blocks_per_split.argtypes = [i32, i32, i32, i32, i32]
+    lib.pkv_choose_kv_blocks_per_split.restype = i32
+    lib.pkv_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.pkv_workspace_size.restype = sz
+    lib.pkv_paged_attention.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32, i32, f32,
+                                        i32, p, sz, p]
+    lib.pkv_paged_attention.restype = ctypes.c_int
+    lib.pkv_attn_combine.argtypes = [p, p, p, p, i32, i32, i32, p]
+    lib.pkv_attn_combine.restype = ctypes.c_int
+    lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    lib.pkv_get_device_error.restype = ctypes.c_int
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    del i64
+    return lib, path
+
+
+_lib, _path = _load()
+
+
+def library_path() -> str:
+    return _path
+
+
+def lib():
+    """The ctypes handle of libpkv.so (for callers that marshal themselves)."""
+    return _lib
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _bf16(t: torch.Tensor, name: str):
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must hold BF16 values (bfloat16 or 16-bit bit patterns), got {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def _i32(t: torch.Tensor, name: str):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+
+
+def _desc(cache: torch.Tensor) -> CacheDesc:
+    if cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks][num_kv_heads][16][128]")
+    nb, hkv, bs, d = cache.shape
+    return CacheDesc(nb, bs, hkv, d)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PkvError(status, where)
+
+
+def kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+              k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    """Store k_new/v_new [T][Hkv][D] into the caches at slot_mapping[T] (int64, <0 skips)."""
+    _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _bf16(k_new, "k_new"), _bf16(v_new, "v_new")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous CUDA int64 tensor")
+    t = slot_mapping.numel()
+    hkv, d = k_cache.shape[1], k_cache.shape[3]
+    if tuple(k_new.shape) != (t, hkv, d) or tuple(v_new.shape) != (t, hkv, d):
+        raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
+    desc = _desc(k_cache)
+    _check(_lib.pkv_kv_append(k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc), slot_mapping.data_ptr(),
+                              k_new.data_ptr(), v_new.data_ptr(), t, _stream_ptr(stream)), "pkv_kv_append")
+
+
+def choose_kv_blocks_per_split(num_seqs: int, num_kv_heads: int, q_len: int, max_blocks_per_seq: int,
+                               sm_count: int = 0) -> int:
+    return int(_lib.pkv_choose_kv_blocks_per_split(num_seqs, num_kv_heads, q_len, max_blocks_per_seq, sm_count))
+
+
+def workspace_size(num_seqs: int, q_len: int, num_q_heads: int, max_blocks_per_seq: int,
+                   kv_blocks_per_split: int, head_dim: int = HEAD_DIM) -> int:
+    return int(_lib.pkv_workspace_size(num_seqs, q_len, num_q_heads, head_dim, max_blocks_per_seq,
+                                       kv_blocks_per_split))
+
+
+def paged_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    block_tables: torch.Tensor, context_lens: torch.Tensor, q_len: int, scale: float,
+                    kv_blocks_per_split: int = 0, workspace: torch.Tensor | None = None, stream=None) -> None:
+    """out[B][q_len][Hq][D] = causal softmax(q K^T * scale) V through the block tables.
+
+    kv_blocks_per_split: 0 = library heuristic; >= max_blocks_per_seq = no
+    split.  When a split is made, `workspace` must be a CUDA tensor of at
+    least workspace_size(...) bytes (256-byte aligned, as torch allocations are).
+    """
+    _bf16(out, "out"), _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    _i32(block_tables, "block_tables"), _i32(context_lens, "context_lens")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
+    b = context_lens.numel()
+    if q.dim() != 4 or q.shape[0] != b or q.shape[1] != q_len or out.shape != q.shape:
+        raise ValueError("q/out must be [num_seqs][q_len][num_q_heads][head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != b:
+        raise ValueError("block_tables must be [num_seqs][max_blocks_per_seq]")
+    hq = q.shape[2]
+    maxb = block_tables.shape[1]
+    desc = _desc(k_cache)
+    bps = kv_blocks_per_split
+    if bps == 0:
+        bps = choose_kv_blocks_per_split(b, desc.num_kv_heads, q_len, maxb)
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(_lib.pkv_paged_attention(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                    ctypes.byref(desc), block_tables.data_ptr(), maxb, context_lens.data_ptr(),
+                                    b, q_len, hq, float(scale), bps, ws_ptr, ws_bytes, _stream_ptr(stream)),
+           "pkv_paged_attention")
+
+
+def attn_combine(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.Tensor,
+                 out_lse: torch.Tensor | None = None, stream=None) -> None:
+    """out[rows][D] (BF16) from partial_o[rows][S][D] and partial_lse[rows][S] (FP32)."""
+    _bf16(out, "out")
+    if partial_o.dtype != torch.float32 or partial_lse.dtype != torch.float32:
+        raise TypeError("partials must be float32")
+    if not (partial_o.is_cuda and partial_lse.is_cuda and partial_o.is_contiguous() and partial_lse.is_contiguous()):
+        raise ValueError("partials must be contiguous CUDA tensors")
+    rows, s, d = partial_o.shape
+    if tuple(partial_lse.shape) != (rows, s) or out.numel() != rows * d:
+        raise ValueError("shape mismatch between out, partial_o and partial_lse")
+    lse_ptr = 0
+    if out_lse is not None:
+        if out_lse.dtype != torch.float32 or out_lse.numel() != rows or not out_lse.is_cuda:
+            raise ValueError("out_lse must be a float32 CUDA tensor of num_rows elements")
+        lse_ptr = out_lse.data_ptr()
+    _check(_lib.pkv_attn_combine(out.data_ptr(), lse_ptr, partial_o.data_ptr(), partial_lse.data_ptr(), rows, d, s,
+                                 _stream_ptr(stream)), "pkv_attn_combine")
+
+
+def get_device_error(reset: bool = True) -> int:
+    """Device error word (DEVERR_* bits) of the current device; synchronises."""
+    word = ctypes.c_uint32(0)
+    _check(_lib.pkv_get_device_error(ctypes.byref(word), 1 if reset else 0), "pkv_get_device_error")
+    return int(word.value)

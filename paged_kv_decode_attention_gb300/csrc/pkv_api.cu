@@ -1,0 +1,210 @@
+// pkv_api.cu -- the exported C ABI of libpkv (declared in include/pkv.h).
+//
+// Host side only: argument validation, the split-KV heuristic, workspace
+// carving and stream-ordered launches.  Nothing here allocates, frees or
+// synchronises device memory (except pkv_get_device_error, which reads the
+// error word and documents that it synchronises).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+#include "pkv_common.cuh"
+#include "pkv_kernels.h"
+
+namespace pkv {
+namespace {
+
+// Device error word (PKV_DEVERR_* bits); one per device that loads the library.
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_error_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+// Address of this device's error word, looked up once per device (with that
+// device current, as cudaGetSymbolAddress requires).
+unsigned int* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (g_error_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_error_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_error_ptr[dev];
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+pkv_status check_cache(const pkv_cache_desc* c) {
+  if (c == nullptr) return PKV_ERR_NULL;
+  if (c->num_blocks < 0 || c->num_kv_heads <= 0) return PKV_ERR_SHAPE;
+  if (c->block_size != kBlockSize || c->head_dim != kHeadDim) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Splits are made only when the un-split grid would leave the GPU
+// under-filled; each split keeps at least this many blocks (256 tokens) so the
+// extra partial-output traffic stays under ~2% of the KV bytes it replaces.
+constexpr int kMinBlocksPerSplit = 16;
+constexpr int kTargetCtasPerSm = 4;
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_NULL: return "PKV_ERR_NULL: a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE: a size is negative or inconsistent";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: shape not supported (block_size 16, head_dim 128, GQA 4)";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: split-KV workspace missing or too small";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA runtime call failed";
+  }
+  return "unknown pkv_status";
+}
+
+pkv_status pkv_kv_append(void* k_cache, void* v_cache, const pkv_cache_desc* cache, const int64_t* slot_mapping,
+                         const void* k_new, const void* v_new, int32_t num_tokens, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !slot_mapping || !k_new || !v_new) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return PKV_ERR_UNSUPPORTED;
+  unsigned int* err = error_word();
+  cudaError_t e = launch_kv_append(k_cache, v_cache, cache->num_blocks, cache->num_kv_heads, slot_mapping,
+                                   k_new, v_new, num_tokens, err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int32_t pkv_choose_kv_blocks_per_split(int32_t num_seqs, int32_t num_kv_heads, int32_t q_len,
+                                       int32_t max_blocks_per_seq, int32_t sm_count) {
+  if (max_blocks_per_seq <= 0) return 1;
+  if (sm_count <= 0) sm_count = device_sm_count();
+  const int64_t rows = static_cast<int64_t>(num_seqs) * (q_len > 0 ? q_len : 1) * num_kv_heads;
+  const int64_t target = static_cast<int64_t>(kTargetCtasPerSm) * sm_count;
+  if (rows <= 0 || rows >= target || max_blocks_per_seq <= kMinBlocksPerSplit) return max_blocks_per_seq;
+  const int64_t splits = (target + rows - 1) / rows;
+  int64_t bps = (max_blocks_per_seq + splits - 1) / splits;
+  if (bps < kMinBlocksPerSplit) bps = kMinBlocksPerSplit;
+  if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
+  return static_cast<int32_t>(bps);
+}
+
+size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t head_dim,
+                          int32_t max_blocks_per_seq, int32_t kv_blocks_per_split) {
+  if (num_seqs <= 0 || q_len <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+      kv_blocks_per_split <= 0 || kv_blocks_per_split >= max_blocks_per_seq)
+    return 0;
+  const size_t splits = (static_cast<size_t>(max_blocks_per_seq) + kv_blocks_per_split - 1) / kv_blocks_per_split;
+  const size_t rows = static_cast<size_t>(num_seqs) * q_len * num_q_heads;
+  return align_up(rows * splits * head_dim * sizeof(float), 256) + align_up(rows * splits * sizeof(float), 256);
+}
+
+pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                               float scale, int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || q_len < 1 || max_blocks_per_seq < 1 || kv_blocks_per_split < 0) return PKV_ERR_SHAPE;
+  if (num_q_heads != kGroup * cache->num_kv_heads) return PKV_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return PKV_ERR_SHAPE;
+  if (static_cast<int64_t>(num_seqs) * q_len > 0x7fffffff || cache->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return PKV_ERR_UNSUPPORTED;
+
+  int32_t bps = kv_blocks_per_split;
+  if (bps == 0)
+    bps = pkv_choose_kv_blocks_per_split(num_seqs, cache->num_kv_heads, q_len, max_blocks_per_seq, 0);
+  if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
+  const int32_t splits = (max_blocks_per_seq + bps - 1) / bps;
+  if (splits > 65535) return PKV_ERR_UNSUPPORTED;
+
+  DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.err = error_word();
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = cache->num_blocks;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.num_seqs = num_seqs;
+  a.q_len = q_len;
+  a.blocks_per_split = bps;
+  a.num_splits = splits;
+  a.scale_log2 = scale * 1.4426950408889634f;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (splits > 1) {
+    const size_t need = pkv_workspace_size(num_seqs, q_len, num_q_heads, kHeadDim, max_blocks_per_seq, bps);
+    if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+    const size_t rows = static_cast<size_t>(num_seqs) * q_len * num_q_heads;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                          align_up(rows * splits * kHeadDim * sizeof(float), 256));
+    if (launch_paged_decode(a, s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), splits, s) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    return PKV_OK;
+  }
+  return launch_paged_decode(a, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_attn_combine(void* out, float* out_lse, const float* partial_o, const float* partial_lse,
+                            int32_t num_rows, int32_t head_dim, int32_t num_splits, void* stream) {
+  if (num_rows < 0 || num_splits < 1) return PKV_ERR_SHAPE;
+  if (head_dim != kHeadDim) return PKV_ERR_UNSUPPORTED;
+  if (num_rows == 0) return PKV_OK;
+  if (!out || !partial_o || !partial_lse) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(out) & 7) || (reinterpret_cast<uintptr_t>(partial_o) & 15) ||
+      (reinterpret_cast<uintptr_t>(partial_lse) & 3))
+    return PKV_ERR_UNSUPPORTED;
+  return launch_attn_combine(out, out_lse, partial_o, partial_lse, num_rows, num_splits,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_get_device_error(uint32_t* host_word, int32_t reset) {
+  if (host_word == nullptr) return PKV_ERR_NULL;
+  unsigned int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return PKV_ERR_CUDA;
+  *host_word = v;
+  if (reset) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

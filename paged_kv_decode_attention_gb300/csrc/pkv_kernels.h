@@ -1,0 +1,41 @@
+// pkv_kernels.h -- host-side launchers of libpkv's kernels (internal).
+// The exported C ABI (pkv_api.cu) validates arguments and calls these.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+// One decode/split launch: grid (rows, splits, kv heads); see paged_decode.cu.
+struct DecodeArgs {
+  void* out;                  // BF16 [B][q_len][Hq][D]; written when num_splits == 1
+  const void* q;              // BF16 [B][q_len][Hq][D]
+  const void* k_cache;        // BF16 [num_blocks][Hkv][16][D]
+  const void* v_cache;
+  const int32_t* block_tables;  // [B][max_blocks]
+  const int32_t* context_lens;  // [B]
+  float* part_o;              // FP32 [B*q_len*Hq][num_splits][D]; used when num_splits > 1
+  float* part_lse;            // FP32 [B*q_len*Hq][num_splits]
+  unsigned int* err;          // device error word
+  int32_t max_blocks;
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  int32_t num_seqs;
+  int32_t q_len;
+  int32_t blocks_per_split;
+  int32_t num_splits;
+  float scale_log2;           // scale * log2(e)
+};
+
+cudaError_t launch_kv_append(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                             const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                             int32_t num_tokens, unsigned int* err, cudaStream_t stream);
+
+cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_attn_combine(void* out, float* out_lse, const float* part_o, const float* part_lse,
+                                int32_t num_rows, int32_t num_splits, cudaStream_t stream);
+
+}  // namespace pkv

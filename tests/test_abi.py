@@ -1,0 +1,112 @@
+"""The C ABI on the host: the library builds and loads, exports every
+function include/pkv.h declares, and rejects bad arguments with the
+documented status before touching the GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_decode_attention_gb300 as pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(pkv_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert {"pkv_kv_append", "pkv_paged_attention", "pkv_attn_combine", "pkv_workspace_size"} <= set(names)
+    lib = ctypes.CDLL(pkv.library_path())
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings():
+    lib = pkv.lib()
+    for code in range(6):
+        assert lib.pkv_status_string(code).startswith(b"PKV_")
+
+
+def test_workspace_size_and_split_heuristic_are_host_arithmetic():
+    lib = pkv.lib()
+    # no split -> no workspace
+    assert lib.pkv_workspace_size(37, 1, 32, 128, 144, 144) == 0
+    rows, splits = 37 * 32, 3
+    need = lib.pkv_workspace_size(37, 1, 32, 128, 144, 48)
+    o_bytes = -(-rows * splits * 128 * 4 // 256) * 256
+    l_bytes = -(-rows * splits * 4 // 256) * 256
+    assert need == o_bytes + l_bytes
+    # a full GPU needs no split; a small batch over a long context does
+    assert lib.pkv_choose_kv_blocks_per_split(512, 8, 1, 144, 152) == 144
+    bps = lib.pkv_choose_kv_blocks_per_split(16, 8, 1, 528, 152)
+    assert 16 <= bps < 528
+    assert lib.pkv_choose_kv_blocks_per_split(1, 8, 1, 8, 152) == 8
+    # the split never goes below 16 blocks
+    assert lib.pkv_choose_kv_blocks_per_split(1, 1, 1, 4096, 152) >= 16
+
+
+def _desc(**kw):
+    d = dict(num_blocks=4, block_size=16, num_kv_heads=8, head_dim=128)
+    d.update(kw)
+    return pkv.CacheDesc(**d)
+
+
+def test_kv_append_argument_errors():
+    lib = pkv.lib()
+    one = ctypes.c_void_p(16)
+    assert lib.pkv_kv_append(one, one, None, one, one, one, 1, None) == 1                       # NULL desc
+    assert lib.pkv_kv_append(one, one, ctypes.byref(_desc(block_size=8)), one, one, one, 1, None) == 3
+    assert lib.pkv_kv_append(one, one, ctypes.byref(_desc(head_dim=64)), one, one, one, 1, None) == 3
+    assert lib.pkv_kv_append(one, one, ctypes.byref(_desc()), one, one, one, -1, None) == 2
+    assert lib.pkv_kv_append(None, one, ctypes.byref(_desc()), one, one, one, 1, None) == 1
+    assert lib.pkv_kv_append(one, one, ctypes.byref(_desc()), one, one, one, 0, None) == 0      # nothing to do
+
+
+def test_paged_attention_argument_errors():
+    lib = pkv.lib()
+    p = ctypes.c_void_p(256)
+    d = ctypes.byref(_desc())
+    args = lambda **kw: dict(dict(out=p, q=p, k=p, v=p, desc=d, bt=p, maxb=4, cl=p, b=2, ql=1, hq=32, scale=0.1,
+                                  bps=4, ws=None, wsb=0, s=None), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return lib.pkv_paged_attention(a["out"], a["q"], a["k"], a["v"], a["desc"], a["bt"], a["maxb"], a["cl"],
+                                       a["b"], a["ql"], a["hq"], a["scale"], a["bps"], a["ws"], a["wsb"], a["s"])
+
+    assert call(desc=None) == 1
+    assert call(out=None) == 1
+    assert call(ql=0) == 2
+    assert call(maxb=0) == 2
+    assert call(b=-1) == 2
+    assert call(hq=16) == 3                        # not 4 query heads per KV head
+    assert call(desc=ctypes.byref(_desc(block_size=32))) == 3
+    assert call(scale=float("nan")) == 2
+    assert call(q=ctypes.c_void_p(258)) == 3       # misaligned
+    assert call(b=0) == 0                          # empty batch: nothing enqueued
+
+
+def test_attn_combine_argument_errors():
+    lib = pkv.lib()
+    p = ctypes.c_void_p(256)
+    assert lib.pkv_attn_combine(p, None, p, p, 4, 64, 2, None) == 3
+    assert lib.pkv_attn_combine(p, None, p, p, 4, 128, 0, None) == 2
+    assert lib.pkv_attn_combine(None, None, p, p, 4, 128, 2, None) == 1
+    assert lib.pkv_attn_combine(p, None, p, p, 0, 128, 2, None) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 8, 16, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkv.kv_append(x, x, torch.zeros(1, dtype=torch.int64), torch.zeros(1, 8, 128, dtype=torch.bfloat16),
+                      torch.zeros(1, 8, 128, dtype=torch.bfloat16))

@@ -1,0 +1,246 @@
+"""CUDA path (through the C ABI) against the FP64 oracle on the same seeded
+inputs.  Append and block-table indexing must be bit-exact; attention must be
+within max-abs 1e-2 and relative L2 5e-3 of the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_util import assert_close, bf16_to_f64, dev, to_device
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import paged_kv_decode_attention_gb300 as pkv
+else:  # collected on CPU-only machines, every test skipped
+    pkv = None
+
+NAN_BF16 = np.uint16(0x7FC0)
+
+
+def run_gpu(w, d=None, bps=0, append=True, out=None):
+    """kv_append (optional) then paged_attention, on device copies; returns (out, device dict)."""
+    if d is None:
+        d = to_device(w)
+    if append:
+        pkv.kv_append(d["k_cache"], d["v_cache"], d["slot_mapping"], d["k_new"], d["v_new"])
+    maxb = w.max_blocks_per_seq
+    if bps == 0:
+        bps = pkv.choose_kv_blocks_per_split(w.num_seqs, w.num_kv_heads, w.q_len, maxb)
+    ws_bytes = pkv.workspace_size(w.num_seqs, w.q_len, w.num_q_heads, maxb, bps)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    if out is None:
+        out = torch.empty_like(d["q"])
+    pkv.paged_attention(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], w.q_len,
+                        w.scale, kv_blocks_per_split=bps, workspace=ws)
+    torch.cuda.synchronize()
+    return out, d
+
+
+def oracle_ref(w, seq_ids=None, append=True):
+    return oracle.run_workload(w, seq_ids=seq_ids, append=append)
+
+
+@pytest.fixture(autouse=True)
+def _clear_device_error():
+    if pkv is not None:
+        pkv.get_device_error(reset=True)
+    yield
+    if pkv is not None:
+        assert pkv.get_device_error(reset=True) == 0
+
+
+# ---------------------------------------------------------------------------
+# kv_append
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("maker", [W.tiny, lambda seed: W.mixed(seed, num_blocks=12000)])
+def test_kv_append_bit_exact(maker):
+    w = maker(seed=1)
+    d = to_device(w)
+    slots = w.slot_mapping.copy()
+    slots[::5] = -1  # padding rows are skipped
+    d["slot_mapping"] = dev(slots)
+    pkv.kv_append(d["k_cache"], d["v_cache"], d["slot_mapping"], d["k_new"], d["v_new"])
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_append(kc, vc, slots, w.k_new, w.v_new)
+    torch.cuda.synchronize()
+    assert np.array_equal(d["k_cache"].cpu().view(torch.int16).numpy().view(np.uint16), kc)
+    assert np.array_equal(d["v_cache"].cpu().view(torch.int16).numpy().view(np.uint16), vc)
+
+
+def test_kv_append_slot_outside_pool_sets_error_and_writes_nothing():
+    w = W.tiny(seed=2)
+    d = to_device(w)
+    slots = w.slot_mapping.copy()
+    slots[0] = w.num_blocks * 16 + 3
+    d["slot_mapping"] = dev(slots)
+    before = d["k_cache"].clone()
+    pkv.kv_append(d["k_cache"], d["v_cache"], d["slot_mapping"], d["k_new"], d["v_new"])
+    assert pkv.get_device_error(reset=True) & pkv.DEVERR_SLOT
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_append(kc, vc, slots, w.k_new, w.v_new)
+    assert np.array_equal(d["k_cache"].cpu().view(torch.int16).numpy().view(np.uint16), kc)
+    assert not torch.equal(before, d["k_cache"])
+
+
+# ---------------------------------------------------------------------------
+# decode attention
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_decode_with_append(seed):
+    w = W.tiny(seed=seed)
+    out, _ = run_gpu(w)
+    assert_close(bf16_to_f64(out), oracle_ref(w), what="tiny")
+
+
+@pytest.mark.parametrize("bps", [1, 2, 3, 5, 16, 1000])
+def test_split_counts_match_oracle_and_each_other(bps):
+    w = W.build("splits", [1, 15, 16, 17, 100, 255, 256, 257, 700], 400, seed=3)
+    ref = oracle_ref(w)
+    out, _ = run_gpu(w, bps=bps)
+    assert_close(bf16_to_f64(out), ref, what=f"bps={bps}")
+
+
+def test_ragged_contexts_padding_rows_and_nan_in_unused_slots():
+    ctx = [0, 1, 2, 3, 7, 15, 16, 17, 31, 33, 0, 64, 65, 129]
+    w = W.build("ragged", ctx, 200, seed=4, max_blocks=12)
+    # every slot no context covers holds NaN: it must never reach a result
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_append(kc, vc, w.slot_mapping, w.k_new, w.v_new)
+    used = np.zeros((w.num_blocks, 16), bool)
+    for r, c in enumerate(ctx):
+        for t in range(c):
+            used[w.block_tables[r, t // 16], t % 16] = True
+    kc.transpose(0, 2, 1, 3)[~used] = NAN_BF16
+    vc.transpose(0, 2, 1, 3)[~used] = NAN_BF16
+    w2 = W.Workload(**{**w.__dict__, "k_cache": kc, "v_cache": vc})
+    ref = oracle_ref(w2, append=False)
+    for bps in (1, 2, 0, 12):
+        out, _ = run_gpu(w2, bps=bps, append=False)
+        got = bf16_to_f64(out)
+        assert (got[np.array(ctx) == 0] == 0).all()
+        assert_close(got, ref, what=f"ragged bps={bps}")
+
+
+def test_physical_placement_bitwise_invariant_at_fixed_split():
+    w = W.build("perm", [40, 300, 129, 77], 120, seed=5)
+    perm = np.random.default_rng(7).permutation(w.num_blocks)
+    inv = np.argsort(perm)
+    w2 = W.Workload(**{**w.__dict__, "k_cache": np.ascontiguousarray(w.k_cache[perm]),
+                       "v_cache": np.ascontiguousarray(w.v_cache[perm]),
+                       "block_tables": inv[w.block_tables].astype(np.int32),
+                       "slot_mapping": np.where(w.slot_mapping >= 0,
+                                                inv[w.slot_mapping // 16] * 16 + w.slot_mapping % 16, -1)})
+    for bps in (3, 19):
+        a, _ = run_gpu(w, bps=bps)
+        b, _ = run_gpu(w2, bps=bps)
+        assert torch.equal(a, b)
+
+
+def test_paged_equals_contiguous_layout():
+    # the same logical sequences laid out contiguously (table = 0,1,2,...)
+    w = W.build("paged", [90, 200, 33], 60, seed=6)
+    need = [-(-int(c) // 16) for c in w.context_lens]
+    order = np.concatenate([w.block_tables[r, :n] for r, n in enumerate(need)])
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_append(kc, vc, w.slot_mapping, w.k_new, w.v_new)
+    tables = np.zeros_like(w.block_tables)
+    base = 0
+    for r, n in enumerate(need):
+        tables[r, :n] = np.arange(base, base + n)
+        base += n
+    w2 = W.Workload(**{**w.__dict__, "k_cache": np.ascontiguousarray(kc[order]),
+                       "v_cache": np.ascontiguousarray(vc[order]), "block_tables": tables})
+    w1 = W.Workload(**{**w.__dict__, "k_cache": kc, "v_cache": vc})
+    a, _ = run_gpu(w1, bps=4, append=False)
+    b, _ = run_gpu(w2, bps=4, append=False)
+    assert torch.equal(a, b)
+
+
+def test_special_cases_ctx1_identical_values_zero_query():
+    # ctx = 1 -> out = v0 exactly (one weight of 1)
+    w = W.build("one", [1, 1, 1], 8, seed=8)
+    out, _ = run_gpu(w)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_append(kc, vc, w.slot_mapping, w.k_new, w.v_new)
+    for r in range(3):
+        blk = w.block_tables[r, 0]
+        for h in range(32):
+            assert np.array_equal(out[r, 0, h].cpu().view(torch.int16).numpy().view(np.uint16), vc[blk, h // 4, 0])
+    # all V rows identical -> that row (to BF16 rounding)
+    w = W.build("same", [50, 300], 30, seed=9)
+    row = W.randn_bf16(np.random.default_rng(3), (8, 128))
+    w.v_cache[:] = row[None, :, None, :]
+    w.v_new[:] = row[None]
+    out, _ = run_gpu(w, bps=5)
+    ref = np.broadcast_to(np.repeat((row.astype(np.uint32) << 16).view(np.float32), 4, axis=0), (2, 1, 32, 128))
+    assert_close(bf16_to_f64(out), ref.astype(np.float64), max_abs=8e-3, what="same-V")
+    # zero query -> mean of values
+    w = W.build("zq", [37, 250], 30, seed=10)
+    w.q[:] = 0
+    out, _ = run_gpu(w, bps=3)
+    assert_close(bf16_to_f64(out), oracle_ref(w), what="zero-q")
+
+
+def test_peaky_logits():
+    w = W.build("peaky", [500, 33, 1000], 120, seed=11)
+    qf = (w.q.astype(np.uint32) << 16).view(np.float32) * 8.0
+    w.q = W.bf16_bits(qf)
+    for bps in (7, 1000):
+        out, _ = run_gpu(w, bps=bps)
+        assert_close(bf16_to_f64(out), oracle_ref(w), what=f"peaky bps={bps}")
+
+
+@pytest.mark.parametrize("q_len", [2, 5, 16])
+def test_chunked_queries_causal(q_len):
+    w = W.build("chunk", [q_len, q_len + 1, 40, 129, 333], 120, q_len=q_len, seed=12)
+    ref = oracle_ref(w)
+    for bps in (2, 0):
+        out, _ = run_gpu(w, bps=bps)
+        assert_close(bf16_to_f64(out), ref, what=f"chunk q_len={q_len} bps={bps}")
+
+
+def test_block_id_outside_pool_sets_error_without_fault():
+    w = W.build("bad", [100, 50], 20, seed=13)
+    w.block_tables[1, 1] = 10_000
+    out, _ = run_gpu(w, bps=2)
+    assert pkv.get_device_error(reset=True) & pkv.DEVERR_BLOCK_ID
+
+
+def test_context_longer_than_table_sets_error():
+    w = W.build("long", [100], 20, seed=14, max_blocks=7)
+    w.context_lens[0] = 7 * 16 + 5
+    run_gpu(w, append=False)
+    assert pkv.get_device_error(reset=True) & pkv.DEVERR_CONTEXT
+
+
+def test_attn_combine_matches_oracle_merge():
+    rng = np.random.default_rng(15)
+    rows, s = 37, 6
+    po = rng.standard_normal((rows, s, 128)).astype(np.float32)
+    pl = (rng.standard_normal((rows, s)) * 3).astype(np.float32)
+    pl[3, 2] = -np.inf
+    pl[5, :] = -np.inf
+    po[3, 2] = np.nan  # an empty split's output is never read
+    ref, ref_lse = oracle.attn_combine(po.astype(np.float64), pl.astype(np.float64))
+    out = torch.empty((rows, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(rows, dtype=torch.float32, device="cuda")
+    pkv.attn_combine(out, dev(po), dev(pl), out_lse=lse)
+    torch.cuda.synchronize()
+    assert_close(bf16_to_f64(out), ref, what="combine")
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    assert np.isneginf(got_lse[5]) and (bf16_to_f64(out)[5] == 0).all()
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(got_lse[fin], ref_lse[fin], rtol=0, atol=1e-5)
+
+
+def test_argument_errors_return_status():
+    w = W.tiny(seed=0)
+    d = to_device(w)
+    out = torch.empty_like(d["q"])
+    with pytest.raises(pkv.PkvError):  # workspace missing for a split call
+        pkv.paged_attention(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], 1,
+                            w.scale, kv_blocks_per_split=1, workspace=None)

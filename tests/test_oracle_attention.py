@@ -241,3 +241,31 @@ def test_workload_shapes():
     assert m.num_seqs == 72 and (m.context_lens[64:] < 16).all()
     c = W.chunk(seed=0, fill_cache=False, num_seqs=8)
     assert ((c.context_lens - 16) % 16 == 0).all() and c.q_len == 16
+
+
+def test_combine_of_range_results_equals_whole_context():
+    # attention over [0, ctx) equals the lse-weighted merge of attention over
+    # block-aligned key ranges, each evaluated by the oracle as its own request
+    w = _small(16, [150, 77, 16])
+    full, full_lse = oracle.paged_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, 1,
+                                            w.scale, with_lse=True)
+    hq, d = w.num_q_heads, 128
+    cuts = [0, 32, 48, 112, 1000]  # token boundaries (multiples of 16); last range may be empty
+    parts_o, parts_l = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        sub_ctx = np.clip(np.minimum(w.context_lens, b) - a, 0, None).astype(np.int32)
+        sub_tables = np.zeros_like(w.block_tables)
+        nb = w.block_tables.shape[1] - a // 16
+        sub_tables[:, :max(nb, 0)] = w.block_tables[:, a // 16:]
+        o, l = oracle.paged_attention(w.q, w.k_cache, w.v_cache, sub_tables, sub_ctx, 1, w.scale, with_lse=True)
+        parts_o.append(o.reshape(-1, d))
+        parts_l.append(l.reshape(-1))
+    po = np.stack(parts_o, axis=1)
+    pl = np.stack(parts_l, axis=1)
+    out, lse = oracle.attn_combine(po, pl)
+    np.testing.assert_allclose(out, full.reshape(-1, d), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, full_lse.reshape(-1), rtol=0, atol=1e-12)
+    assert hq == 8
+    # a row whose ranges are all empty merges to zeros
+    z, zl = oracle.attn_combine(np.ones((1, 3, 4)), np.full((1, 3), -np.inf))
+    assert (z == 0).all() and np.isneginf(zl).all()

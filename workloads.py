@@ -282,3 +282,22 @@ def sweep_point(num_seqs: int, ctx: int, seed: int = 0, fill_cache: bool = True)
 
 SWEEP_BATCHES = [1 << i for i in range(10)]           # 1 .. 512
 SWEEP_CONTEXTS = [128 << i for i in range(10)]        # 128 .. 65536
+
+
+def fill_pool_device(cache, seed: int, chunk_blocks: int = 8192) -> None:
+    """Fill a device pool tensor [num_blocks][Hkv][16][D] (BF16) with seeded
+    N(0,1) values drawn by torch's device generator, chunk by chunk (for pools
+    too large to draw on the host).  Same recipe as randn_bf16: float32 draws
+    rounded to BF16 (torch's conversion rounds to nearest even)."""
+    import torch
+
+    gen = torch.Generator(device=cache.device)
+    gen.manual_seed(int(seed))
+    flat = cache.view(cache.shape[0], -1)
+    tmp = None
+    for b0 in range(0, cache.shape[0], chunk_blocks):
+        b1 = min(cache.shape[0], b0 + chunk_blocks)
+        if tmp is None or tmp.shape[0] != b1 - b0:
+            tmp = torch.empty((b1 - b0, flat.shape[1]), dtype=torch.float32, device=cache.device)
+        tmp.normal_(generator=gen)
+        flat[b0:b1].copy_(tmp.to(torch.bfloat16).view(flat.dtype))
