@@ -213,7 +213,7 @@ def time_oracle(sub, budget_s: float = 12.0, max_reps: int = 200):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="short", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--seed", type=int, default=0)
@@ -223,11 +223,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--oracle-budget-s", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world, rank, local = dist_init(args.gpus)
     w, layers = make_workload(args.workload, args.seed)
+    if args.layers > 0:
+        layers = args.layers
     attn_b, app_b = bytes_per_layer(w)
     step_bytes = layers * (attn_b + app_b)
     tokens_layers = int(w.context_lens.sum()) * w.q_len * layers if w.q_len > 1 else int(w.context_lens.sum()) * layers
