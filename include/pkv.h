@@ -154,6 +154,41 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
                                int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Bytes of the scratch array compiled into libpkv for
+ * pkv_paged_attention_static_workspace (held on every GPU that loads the
+ * library, until the process exits). */
+#define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * pkv_paged_attention_static_workspace -- pkv_paged_attention for callers
+ * that cannot allocate device memory.  The pages have no counterpart to this
+ * entry point; it exists for callers that may not enter a device allocator:
+ * code running inside a memory manager or an allocation hook, under a
+ * framework that forbids allocation on its hot path, or plain C callers that
+ * hold no CUDA allocator.
+ *
+ * Arguments and results are those of pkv_paged_attention, minus the
+ * workspace: split-KV partials go to one scratch array of
+ * PKV_STATIC_WORKSPACE_BYTES inside the library, on the current device.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine.  The caller still provides inputs and outputs.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents.  Nothing in it must start at zero.  Calls that can overlap on
+ *     the GPU (unordered streams) race on it: order them.
+ *   - Returns PKV_ERR_WORKSPACE, enqueuing nothing, when the resolved split
+ *     needs more than PKV_STATIC_WORKSPACE_BYTES (pkv_workspace_size tells
+ *     the need); a larger kv_blocks_per_split needs less.
+ */
+pkv_status pkv_paged_attention_static_workspace(void* out, const void* q, const void* k_cache,
+                                                const void* v_cache, const pkv_cache_desc* cache,
+                                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                const int32_t* context_lens, int32_t num_seqs,
+                                                int32_t q_len, int32_t num_q_heads, float scale,
+                                                int32_t kv_blocks_per_split, void* stream);
+
 /*
  * pkv_attn_combine -- merge split-KV partial results (the log-sum-exp
  * identity of blockwise softmax: a softmax over the union of key ranges is
