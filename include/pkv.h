@@ -105,11 +105,12 @@ int32_t pkv_choose_kv_blocks_per_split(int32_t num_seqs, int32_t num_kv_heads, i
 
 /*
  * pkv_workspace_size -- bytes of device workspace pkv_paged_attention needs
- * for these sizes and this (already resolved, > 0) kv_blocks_per_split; 0 when
- * no split is made.  Layout: partial_o FP32 [num_seqs][q_len][num_q_heads]
+ * for these sizes and this (already resolved, > 0) kv_blocks_per_split.  With
+ * num_splits = ceil(max_blocks_per_seq / kv_blocks_per_split): 0 when
+ * num_splits <= 8 (one split, or splits merged on chip inside a thread-block
+ * cluster); otherwise partial_o FP32 [num_seqs][q_len][num_q_heads]
  * [num_splits][head_dim], then partial_lse FP32 [num_seqs][q_len][num_q_heads]
- * [num_splits], with num_splits = ceil(max_blocks_per_seq / kv_blocks_per_split),
- * each part 256-byte aligned.
+ * [num_splits], each part 256-byte aligned.
  */
 size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t head_dim,
                           int32_t max_blocks_per_seq, int32_t kv_blocks_per_split);
@@ -139,10 +140,12 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, 
  *   kv_blocks_per_split : 0 = choose with pkv_choose_kv_blocks_per_split;
  *                  >= max_blocks_per_seq = one pass per (request, kv head);
  *                  otherwise each request's blocks are reduced in ranges of
- *                  this many blocks and merged by the combine kernel.
+ *                  this many blocks and the ranges merged: on chip (one
+ *                  thread-block cluster per row) for up to 8 ranges, else
+ *                  through the workspace and the combine kernel.
  *   workspace, workspace_bytes : device scratch of at least
  *                  pkv_workspace_size(...) bytes for the resolved split (may be
- *                  NULL/0 when no split is made).  Its contents are
+ *                  NULL/0 when that size is 0).  Its contents are
  *                  overwritten; calls that share it must be stream-ordered.
  * The result does not depend on where blocks sit in the pool; with a fixed
  * split it is bitwise reproducible.  The split changes rounding only.

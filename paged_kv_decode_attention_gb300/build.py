@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "libpkv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", f"-I{INCLUDE}", f"-I{CSRC}",
-                     "--expt-relaxed-constexpr"]
+                     "--expt-relaxed-constexpr"] + os.environ.get("PKV_NVCC_FLAGS", "").split()
 
 
 def _nvcc() -> str:

@@ -57,10 +57,11 @@ pkv_status check_cache(const pkv_cache_desc* c) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Splits are made only when the un-split grid would leave the GPU
-// under-filled; each split keeps at least this many blocks (256 tokens) so the
-// extra partial-output traffic stays under ~2% of the KV bytes it replaces.
+// under-filled: the decode kernel keeps 2 CTAs per SM busy, and one full wave
+// of long-running CTAs beats several waves of short ones (each CTA pays a
+// pipeline fill).  Each split keeps at least 16 blocks (256 tokens).
 constexpr int kMinBlocksPerSplit = 16;
-constexpr int kTargetCtasPerSm = 4;
+constexpr int kResidentCtasPerSm = 2;
 
 }  // namespace
 }  // namespace pkv
@@ -102,9 +103,10 @@ int32_t pkv_choose_kv_blocks_per_split(int32_t num_seqs, int32_t num_kv_heads, i
   if (max_blocks_per_seq <= 0) return 1;
   if (sm_count <= 0) sm_count = device_sm_count();
   const int64_t rows = static_cast<int64_t>(num_seqs) * (q_len > 0 ? q_len : 1) * num_kv_heads;
-  const int64_t target = static_cast<int64_t>(kTargetCtasPerSm) * sm_count;
-  if (rows <= 0 || rows >= target || max_blocks_per_seq <= kMinBlocksPerSplit) return max_blocks_per_seq;
-  const int64_t splits = (target + rows - 1) / rows;
+  const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
+  if (rows <= 0 || max_blocks_per_seq <= kMinBlocksPerSplit) return max_blocks_per_seq;
+  const int64_t splits = (slots + rows / 2) / rows;  // nearest whole number of splits to one wave
+  if (splits <= 1) return max_blocks_per_seq;
   int64_t bps = (max_blocks_per_seq + splits - 1) / splits;
   if (bps < kMinBlocksPerSplit) bps = kMinBlocksPerSplit;
   if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
@@ -117,6 +119,7 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, 
       kv_blocks_per_split <= 0 || kv_blocks_per_split >= max_blocks_per_seq)
     return 0;
   const size_t splits = (static_cast<size_t>(max_blocks_per_seq) + kv_blocks_per_split - 1) / kv_blocks_per_split;
+  if (splits <= static_cast<size_t>(kMaxClusterSplits)) return 0;  // merged inside a thread-block cluster
   const size_t rows = static_cast<size_t>(num_seqs) * q_len * num_q_heads;
   return align_up(rows * splits * head_dim * sizeof(float), 256) + align_up(rows * splits * sizeof(float), 256);
 }
@@ -163,7 +166,7 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (splits > 1) {
+  if (splits > kMaxClusterSplits) {
     const size_t need = pkv_workspace_size(num_seqs, q_len, num_q_heads, kHeadDim, max_blocks_per_seq, bps);
     if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;

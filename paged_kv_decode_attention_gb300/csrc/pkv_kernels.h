@@ -8,6 +8,11 @@
 
 namespace pkv {
 
+// Splits of one (row, KV head) up to this count run as one thread-block
+// cluster and merge through distributed shared memory (no workspace); more
+// splits go through the workspace and the combine kernel.
+constexpr int kMaxClusterSplits = 8;
+
 // One decode/split launch: grid (rows, splits, kv heads); see paged_decode.cu.
 struct DecodeArgs {
   void* out;                  // BF16 [B][q_len][Hq][D]; written when num_splits == 1
@@ -16,7 +21,7 @@ struct DecodeArgs {
   const void* v_cache;
   const int32_t* block_tables;  // [B][max_blocks]
   const int32_t* context_lens;  // [B]
-  float* part_o;              // FP32 [B*q_len*Hq][num_splits][D]; used when num_splits > 1
+  float* part_o;              // FP32 [B*q_len*Hq][num_splits][D]; NULL = cluster merge
   float* part_lse;            // FP32 [B*q_len*Hq][num_splits]
   unsigned int* err;          // device error word
   int32_t max_blocks;
@@ -33,6 +38,8 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, int32_t num_blocks, i
                              const int64_t* slot_mapping, const void* k_new, const void* v_new,
                              int32_t num_tokens, unsigned int* err, cudaStream_t stream);
 
+// num_splits == 1: direct; part_o == NULL: cluster merge (num_splits <= kMaxClusterSplits);
+// otherwise partials to the workspace (the caller then runs the combine kernel).
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_attn_combine(void* out, float* out_lse, const float* part_o, const float* part_lse,

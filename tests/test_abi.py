@@ -40,8 +40,11 @@ def test_workspace_size_and_split_heuristic_are_host_arithmetic():
     lib = pkv.lib()
     # no split -> no workspace
     assert lib.pkv_workspace_size(37, 1, 32, 128, 144, 144) == 0
-    rows, splits = 37 * 32, 3
-    need = lib.pkv_workspace_size(37, 1, 32, 128, 144, 48)
+    # up to 8 splits merge inside a thread-block cluster: no workspace
+    assert lib.pkv_workspace_size(37, 1, 32, 128, 144, 48) == 0
+    assert lib.pkv_workspace_size(37, 1, 32, 128, 144, 18) == 0
+    rows, splits = 37 * 32, 9
+    need = lib.pkv_workspace_size(37, 1, 32, 128, 144, 16)
     o_bytes = -(-rows * splits * 128 * 4 // 256) * 256
     l_bytes = -(-rows * splits * 4 // 256) * 256
     assert need == o_bytes + l_bytes
