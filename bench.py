@@ -44,7 +44,7 @@ KV_BYTES_PER_TOKEN = 2 * W.NUM_KV_HEADS * W.HEAD_DIM * 2  # K and V of one token
 # workload selection
 # ---------------------------------------------------------------------------
 
-def make_workload(name: str, seed: int):
+def make_workload(name: str, seed: int, num_seqs: int = 0):
     if name == "short":
         return W.short_chat(seed=seed, fill_cache=False), W.NUM_LAYERS
     if name == "long":
@@ -52,7 +52,7 @@ def make_workload(name: str, seed: int):
     if name == "mixed":
         return W.mixed(seed=seed, fill_cache=False), W.NUM_LAYERS
     if name == "chunk":
-        return W.chunk(seed=seed, fill_cache=False), 1
+        return W.chunk(seed=seed, fill_cache=False, **({"num_seqs": num_seqs} if num_seqs else {})), 1
     if name == "tiny":
         return W.tiny(seed=seed, fill_cache=False), W.NUM_LAYERS
     raise SystemExit(f"unknown workload {name}")
@@ -224,11 +224,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--oracle-budget-s", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
+    ap.add_argument("--num-seqs", type=int, default=0, help="chunk workload: fewer requests (small profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world, rank, local = dist_init(args.gpus)
-    w, layers = make_workload(args.workload, args.seed)
+    w, layers = make_workload(args.workload, args.seed, args.num_seqs)
     if args.layers > 0:
         layers = args.layers
     attn_b, app_b = bytes_per_layer(w)

@@ -1,0 +1,455 @@
+// paged_chunk_tc.cu -- causal chunk attention on the 5th-generation tensor
+// cores: 64 query rows (16 query positions x the 4 query heads of a GQA
+// group) against the request's paged K/V, one KV head per CTA.
+//
+// What it computes ("Chapter 8: Inference Optimization",
+// clxhxhhr.top/posts/4341): §8.2.3 and Fig. 8-8/8-9 -- of c new tokens after
+// h cached ones, new token j attends to the first h + j tokens; §8.3.1 /
+// Fig. 8-10 -- every K/V block is found through the request's block table;
+// §8.5.2 -- verifying several positions reads the same KV.  With 16 positions
+// x 4 heads the work is a dense contraction (64 rows against every 16-token
+// tile), so S = Q K^T and O = P V run as tcgen05.mma with FP32 accumulators in
+// tensor memory, and softmax runs in FP32 on the CUDA cores in between.
+//
+// CTA = 6 warps, one (request, row tile, split, KV head):
+//   warp 0  : TMA producer.  A KV tile is 4 blocks (64 tokens): for each block
+//             two 16x64 boxes of K and two of V (128-byte swizzle) land in a
+//             2-stage ring; blocks past the range are fetched at an
+//             out-of-range row so TMA fills them with zeros.
+//   warp 1  : MMA issuer (one thread).  S_j = Q K_j^T (M 64, N 64, 8 k-steps)
+//             into a double-buffered TMEM S; O += P_j V_j (M 64, N 128, 4
+//             k-steps) into TMEM O.  S_{j+1} is issued before waiting for P_j
+//             so QK^T overlaps the softmax.
+//   warps 2-5: softmax.  Thread = one row (TMEM lanes 0-15 of each 32-lane
+//             sub-partition hold the M=64 accumulator).  Scores are masked
+//             (causal and context), scaled into base 2, exponentiated against
+//             a lazily updated row max (O in TMEM is rescaled only when a row
+//             max grows by more than 2^8), written as BF16 P into a 128-byte
+//             swizzled shared tile, and handed to the MMA warp.
+//   epilogue: O / l to BF16 (one split) or FP32 + lse (split-KV partials).
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pkv_common.cuh"
+#include "pkv_kernels.h"
+#include "pkv_tcgen05.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kTcStages = 2;
+constexpr int kTileBlocks = 4;                        // KV blocks per tile
+constexpr int kTileTokens = kTileBlocks * kBlockSize;  // 64
+constexpr int kRows = 64;                             // 16 positions x 4 heads
+constexpr int kQBytes = kRows * kHeadDim * 2;         // 16 KiB
+constexpr int kPBytes = kRows * kTileTokens * 2;      // 8 KiB
+constexpr int kHalfBytes = kTileTokens * 128;         // 64 tokens x 64 dims = 8 KiB
+constexpr int kStageBytesTc = 4 * kHalfBytes;         // K lo/hi, V lo/hi: 32 KiB
+constexpr int kOffQ = 0;
+constexpr int kOffP = kOffQ + kQBytes;
+constexpr int kOffKV = kOffP + 2 * kPBytes;
+constexpr int kOffBar = kOffKV + kTcStages * kStageBytesTc;
+constexpr int kSmemTc = kOffBar + 256;
+constexpr uint32_t kTmemCols = 256;  // S0 [0,64), S1 [64,128), O [128,256)
+constexpr uint32_t kColO = 128;
+constexpr float kRescaleThreshold = 8.f;  // log2 units: weights stay below 2^8
+constexpr float kLn2 = 0.6931471805599453f;
+
+static_assert(kSmemTc <= 113 * 1024, "two CTAs per SM");
+
+struct TcBars {
+  uint64_t kv_full[kTcStages];
+  uint64_t kv_empty[kTcStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint32_t tmem_base;
+};
+static_assert(sizeof(TcBars) <= 256, "barrier area");
+
+template <bool kSplit>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    paged_chunk_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                          const ChunkArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  TcBars* bars = reinterpret_cast<TcBars*>(smem + kOffBar);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int n_rt = (a.q_len + 15) / 16;   // row tiles per request
+  const int r = blockIdx.x / n_rt;
+  const int rt = blockIdx.x - r * n_rt;
+  const int split = blockIdx.y;
+  const int kvh = blockIdx.z;
+  const int hq = a.num_kv_heads * kGroup;
+  const int ctx = a.context_lens[r];
+  const int cap = a.max_blocks * kBlockSize;
+  if (ctx > cap && threadIdx.x == 0 && split == 0 && kvh == 0 && rt == 0) report(a.err, PKV_DEVERR_CONTEXT);
+  // last position of this row tile and the keys it sees (the most of any row here)
+  const int ip_last = min(a.q_len - 1, rt * 16 + 15);
+  int n_vis_cta = ctx - a.q_len + 1 + ip_last;
+  if (ctx <= 0 || n_vis_cta < 0) n_vis_cta = 0;
+  n_vis_cta = min(n_vis_cta, cap);
+  const int ctx_keys = min(max(ctx, 0), cap);  // keys that hold data (the rest of a block may be garbage)
+  const int nb = (n_vis_cta + kBlockSize - 1) / kBlockSize;
+  const int b0 = split * a.blocks_per_split;
+  const int b1 = min(nb, b0 + a.blocks_per_split);
+  const int n_tiles = (b1 - b0 + kTileBlocks - 1) / kTileBlocks;
+
+  // rows handled by softmax threads: warp w >= 2 owns TMEM sub-partition w % 4
+  const int quad = warp & 3;
+  const int row = quad * 16 + lane;  // meaningful for lane < 16
+  const int ip = rt * 16 + (row >> 2);
+  const int g = row & 3;
+  const bool row_valid = warp >= 2 && lane < 16 && ip < a.q_len;
+  const int64_t orow = (static_cast<int64_t>(r) * a.q_len + ip) * hq + kvh * kGroup + g;
+
+  if (n_tiles <= 0) {
+    if (row_valid) {
+      if constexpr (kSplit) {
+        a.part_lse[orow * a.num_splits + split] = -INFINITY;
+      } else {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < kHeadDim * 2 / 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    return;
+  }
+
+  // ---------------- set-up: barriers, TMEM, Q tile ----------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->o_done[s], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tensor_map(&k_map);
+    tc::prefetch_tensor_map(&v_map);
+  }
+  if (warp >= 2) {
+    // Q rows (position, head) -> 128-byte swizzled K-major tile, two 64-dim halves
+    const int t = threadIdx.x - 64;  // 0..127
+    const uint16_t* qbase = static_cast<const uint16_t*>(a.q);
+    for (int idx = t; idx < kRows * 16; idx += 128) {
+      const int m = idx >> 4;
+      const int ch = idx & 15;  // 16-byte chunk of the row
+      const int ipm = rt * 16 + (m >> 2);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (ipm < a.q_len)
+        v = *reinterpret_cast<const uint4*>(
+            qbase + ((static_cast<int64_t>(r) * a.q_len + ipm) * hq + kvh * kGroup + (m & 3)) * kHeadDim + ch * 8);
+      const int half = ch >> 3;
+      *reinterpret_cast<uint4*>(smem + kOffQ + half * 8192 + tc::sw128_offset(m, (ch & 7) * 8)) = v;
+    }
+    tc::fence_proxy_async_smem();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t sbase = smem_addr(smem);
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------------------- TMA producer ----------------------------
+    const uint64_t policy = l2_policy_evict_first();
+    const int32_t* table = a.block_tables + static_cast<int64_t>(r) * a.max_blocks;
+    const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;  // first row past the pool
+    const int n_blocks = b1 - b0;
+    for (int base = 0; base < n_tiles * kTileBlocks && ok; base += 32) {
+      int y = oob_row;
+      if (base + lane < n_blocks) {
+        int blk = table[b0 + base + lane];
+        if (blk < 0 || blk >= a.num_blocks) {
+          report(a.err, PKV_DEVERR_BLOCK_ID);
+          blk = 0;
+        }
+        y = (blk * a.num_kv_heads + kvh) * kBlockSize;
+      }
+      const int cnt = min(32, n_tiles * kTileBlocks - base);
+      for (int u = 0; u < cnt; ++u) {
+        const int yy = __shfl_sync(0xffffffffu, y, u);
+        const int bi = base + u;
+        const int j = bi / kTileBlocks;
+        const int b = bi % kTileBlocks;
+        const int st = j % kTcStages;
+        if (lane == 0) {
+          if (b == 0) {
+            if (j >= kTcStages) ok = mbar_wait(&bars->kv_empty[st], ((j / kTcStages) & 1) ^ 1);
+            if (ok) mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytesTc);
+          }
+          if (ok) {
+            uint8_t* stg = smem + kOffKV + st * kStageBytesTc;
+            tc::tma_load_2d(stg + 0 * kHalfBytes + b * 2048, &k_map, 0, yy, &bars->kv_full[st], policy);
+            tc::tma_load_2d(stg + 1 * kHalfBytes + b * 2048, &k_map, 64, yy, &bars->kv_full[st], policy);
+            tc::tma_load_2d(stg + 2 * kHalfBytes + b * 2048, &v_map, 0, yy, &bars->kv_full[st], policy);
+            tc::tma_load_2d(stg + 3 * kHalfBytes + b * 2048, &v_map, 64, yy, &bars->kv_full[st], policy);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+    }
+    if (lane == 0) {
+      if (!ok) report(a.err, PKV_DEVERR_TIMEOUT);
+      // the last tiles' copies must land before shared memory is released
+      for (int j = max(0, n_tiles - kTcStages); j < n_tiles; ++j)
+        mbar_wait(&bars->kv_full[j % kTcStages], (j / kTcStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------- MMA issuer ----------------------------
+    if (lane == 0) {
+      constexpr uint32_t kIdS = tc::idesc_bf16_f32(kRows, kTileTokens, false, false);
+      constexpr uint32_t kIdO = tc::idesc_bf16_f32(kRows, kHeadDim, false, true);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kTcStages;
+        const int sb = j & 1;
+        if (!mbar_wait(&bars->kv_full[st], (j / kTcStages) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&bars->p_full[sb], ((j - 2) >> 1) & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t kst = sbase + kOffKV + st * kStageBytesTc;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t qa = sbase + kOffQ + (kk >> 2) * 8192 + 32 * (kk & 3);
+          const uint32_t ka = kst + (kk >> 2) * kHalfBytes + 32 * (kk & 3);
+          tc::mma_bf16(tmem + sb * 64, tc::smem_desc(qa, 16, 1024), tc::smem_desc(ka, 16, 1024), kIdS, kk > 0);
+        }
+        tc::commit(&bars->s_full[sb]);
+        return true;
+      };
+      ok = issue_s(0);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        if (j + 1 < n_tiles) ok = issue_s(j + 1);
+        if (ok) ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const int st = j % kTcStages;
+        const uint32_t pst = sbase + kOffP + (j & 1) * kPBytes;
+        const uint32_t vst = sbase + kOffKV + st * kStageBytesTc + 2 * kHalfBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          tc::mma_bf16(tmem + kColO, tc::smem_desc(pst + 32 * kk, 16, 1024),
+                       tc::smem_desc(vst + 2048 * kk, kHalfBytes, 1024), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(&bars->o_done[j & 1]);
+        tc::commit(&bars->kv_empty[st]);
+      }
+      if (!ok) report(a.err, PKV_DEVERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------- softmax ----------------------------
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    // keys this row may see inside this split: causal limit, context, and the
+    // split's own block range (the tail tile's extra blocks arrive zero-filled)
+    const int n_vis_row = row_valid ? min(min(max(ctx - a.q_len + 1 + ip, 0), cap), b1 * kBlockSize) : 0;
+    float m_stale = -INFINITY;  // max the weights are taken against (lags the true max by < 2^8)
+    float l = 0.f;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int sb = j & 1;
+      const int st = j % kTcStages;
+      // keep `ok` warp-uniform: the tcgen05 loads below are warp-collective
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j >> 1) & 1));
+      if (!ok) break;
+      tc::fence_after_sync();
+      float s[kTileTokens];
+      tc::tmem_ld32(tmem + lane_off + sb * 64, s);
+      tc::tmem_ld32(tmem + lane_off + sb * 64 + 32, s + 32);
+      tc::tmem_wait_ld();
+      const int tok0 = (b0 + j * kTileBlocks) * kBlockSize;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTileTokens; ++c) {
+        s[c] = (tok0 + c < n_vis_row) ? s[c] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[c]);
+      }
+      const bool grow = mx > m_stale + kRescaleThreshold;  // also true the first time a row sees a key
+      const float m_new = grow ? mx : m_stale;
+      const float alpha = grow ? exp2_approx(m_stale - m_new) : 1.f;  // 0 while m_stale is -inf
+      if (__any_sync(0xffffffffu, grow && j > 0 && m_stale != -INFINITY)) {
+        // O holds weights taken against the old maxima: rescale this warp's rows
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1));
+        tc::fence_after_sync();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tc::tmem_ld32(tmem + lane_off + kColO + 32 * cc, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tc::tmem_st32(tmem + lane_off + kColO + 32 * cc, o);
+        }
+        tc::tmem_wait_st();
+      }
+      l *= alpha;
+      m_stale = m_new;
+      const float m_use = (m_stale == -INFINITY) ? 0.f : m_stale;
+      // P buffer sb was last read by PV_{j-2}
+      if (j >= 2) ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars->o_done[sb], ((j - 2) >> 1) & 1));
+      uint8_t* prow = smem + kOffP + sb * kPBytes;
+      float rs = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = exp2_approx(s[cc * 8 + e] - m_use);
+          rs += p[e];
+        }
+        if (lane < 16) {
+          uint4 w;
+          w.x = pack_bf16x2(p[0], p[1]);
+          w.y = pack_bf16x2(p[2], p[3]);
+          w.z = pack_bf16x2(p[4], p[5]);
+          w.w = pack_bf16x2(p[6], p[7]);
+          *reinterpret_cast<uint4*>(prow + tc::sw128_offset(row, cc * 8)) = w;
+        }
+      }
+      l += rs;
+      // slots past the request's data in its last block may hold anything: zero those V rows
+      const int tile_end = tok0 + kTileTokens;
+      if (ctx_keys < tile_end && ctx_keys > tok0 && (ctx_keys & (kBlockSize - 1)) != 0) {
+        const int first = ctx_keys - tok0;                                // first garbage token of the tile
+        const int last = min(kTileTokens, ((first + kBlockSize - 1) / kBlockSize) * kBlockSize);
+        uint8_t* vt = smem + kOffKV + st * kStageBytesTc + 2 * kHalfBytes;
+        const int t128 = threadIdx.x - 64;
+        for (int idx = t128; idx < (last - first) * 16; idx += 128) {
+          const int tk = first + (idx >> 4);
+          const int ch = idx & 15;  // 8 chunks in each 64-dim half
+          *reinterpret_cast<uint4*>(vt + (ch >> 3) * kHalfBytes + tk * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(&bars->p_full[sb]);
+    }
+    if (!ok && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
+    // ---- epilogue ----
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1));
+    tc::fence_after_sync();
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    const float lse = (l > 0.f) ? (m_stale + log2f(l)) * kLn2 : -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float o[32];
+      tc::tmem_ld32(tmem + lane_off + kColO + 32 * cc, o);
+      tc::tmem_wait_ld();
+      if (row_valid && ok) {
+        if constexpr (kSplit) {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + (orow * a.num_splits + split) * kHeadDim + 32 * cc);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim + 32 * cc);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = pack_bf16x2(o[8 * e] * inv, o[8 * e + 1] * inv);
+            w.y = pack_bf16x2(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
+            w.z = pack_bf16x2(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
+            w.w = pack_bf16x2(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
+            dst[e] = w;
+          }
+        }
+      }
+    }
+    if constexpr (kSplit) {
+      if (row_valid && ok) a.part_lse[orow * a.num_splits + split] = lse;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side: tensor maps over a KV pool viewed as rows of 128 BF16
+// ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kSplit>
+cudaError_t allow_smem_tc() {
+  static bool done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(paged_chunk_tc_kernel<kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;
+  if (rows + kBlockSize >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  CUtensorMap kmap, vmap;
+  if (!make_pool_map(&kmap, a.k_cache, rows) || !make_pool_map(&vmap, a.v_cache, rows)) return cudaErrorInvalidValue;
+  const int n_rt = (a.q_len + 15) / 16;
+  const dim3 grid(static_cast<unsigned>(a.num_seqs * n_rt), static_cast<unsigned>(a.num_splits),
+                  static_cast<unsigned>(a.num_kv_heads));
+  if (grid.x == 0) return cudaSuccess;
+  cudaError_t e;
+  if (a.num_splits > 1) {
+    if ((e = allow_smem_tc<true>()) != cudaSuccess) return e;
+    paged_chunk_tc_kernel<true><<<grid, kTcThreads, kSmemTc, stream>>>(kmap, vmap, a);
+  } else {
+    if ((e = allow_smem_tc<false>()) != cudaSuccess) return e;
+    paged_chunk_tc_kernel<false><<<grid, kTcThreads, kSmemTc, stream>>>(kmap, vmap, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -62,6 +62,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // pipeline fill).  Each split keeps at least 16 blocks (256 tokens).
 constexpr int kMinBlocksPerSplit = 16;
 constexpr int kResidentCtasPerSm = 2;
+constexpr int kTcMinBlocksPerSplit = 128;
 
 }  // namespace
 }  // namespace pkv
@@ -101,6 +102,13 @@ pkv_status pkv_kv_append(void* k_cache, void* v_cache, const pkv_cache_desc* cac
 int32_t pkv_choose_kv_blocks_per_split(int32_t num_seqs, int32_t num_kv_heads, int32_t q_len,
                                        int32_t max_blocks_per_seq, int32_t sm_count) {
   if (max_blocks_per_seq <= 0) return 1;
+  if (q_len >= kTcMinQLen) {
+    // tensor-core chunk kernel: cap each CTA at ~1/8 of the longest request
+    // (and never below 2048 tokens) so one long request cannot form the tail
+    if (max_blocks_per_seq <= kTcMinBlocksPerSplit) return max_blocks_per_seq;
+    int32_t bps = (max_blocks_per_seq + 7) / 8;
+    return bps < kTcMinBlocksPerSplit ? kTcMinBlocksPerSplit : bps;
+  }
   if (sm_count <= 0) sm_count = device_sm_count();
   const int64_t rows = static_cast<int64_t>(num_seqs) * (q_len > 0 ? q_len : 1) * num_kv_heads;
   const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
@@ -119,7 +127,8 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, 
       kv_blocks_per_split <= 0 || kv_blocks_per_split >= max_blocks_per_seq)
     return 0;
   const size_t splits = (static_cast<size_t>(max_blocks_per_seq) + kv_blocks_per_split - 1) / kv_blocks_per_split;
-  if (splits <= static_cast<size_t>(kMaxClusterSplits)) return 0;  // merged inside a thread-block cluster
+  if (q_len < kTcMinQLen && splits <= static_cast<size_t>(kMaxClusterSplits))
+    return 0;  // decode splits merge inside a thread-block cluster
   const size_t rows = static_cast<size_t>(num_seqs) * q_len * num_q_heads;
   return align_up(rows * splits * head_dim * sizeof(float), 256) + align_up(rows * splits * sizeof(float), 256);
 }
@@ -166,7 +175,8 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (splits > kMaxClusterSplits) {
+  const bool tensor_cores = q_len >= kTcMinQLen;
+  if (splits > kMaxClusterSplits || (tensor_cores && splits > 1)) {
     const size_t need = pkv_workspace_size(num_seqs, q_len, num_q_heads, kHeadDim, max_blocks_per_seq, bps);
     if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
@@ -174,12 +184,14 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
     a.part_o = static_cast<float*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                           align_up(rows * splits * kHeadDim * sizeof(float), 256));
-    if (launch_paged_decode(a, s) != cudaSuccess) return PKV_ERR_CUDA;
+    if ((tensor_cores ? launch_paged_chunk_tc(a, s) : launch_paged_decode(a, s)) != cudaSuccess)
+      return PKV_ERR_CUDA;
     if (launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), splits, s) != cudaSuccess)
       return PKV_ERR_CUDA;
     return PKV_OK;
   }
-  return launch_paged_decode(a, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return (tensor_cores ? launch_paged_chunk_tc(a, s) : launch_paged_decode(a, s)) == cudaSuccess ? PKV_OK
+                                                                                                 : PKV_ERR_CUDA;
 }
 
 pkv_status pkv_attn_combine(void* out, float* out_lse, const float* partial_o, const float* partial_lse,

@@ -42,6 +42,15 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, int32_t num_blocks, i
 // otherwise partials to the workspace (the caller then runs the combine kernel).
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// Queries per request at or above which the tensor-core chunk kernel runs
+// (16 positions x 4 heads = 64 rows, one tcgen05 M=64 tile).
+constexpr int kTcMinQLen = 16;
+
+// Chunked causal attention on tensor cores (paged_chunk_tc.cu).  Same fields
+// as DecodeArgs; num_splits > 1 always goes through the workspace.
+using ChunkArgs = DecodeArgs;
+cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
+
 cudaError_t launch_attn_combine(void* out, float* out_lse, const float* part_o, const float* part_lse,
                                 int32_t num_rows, int32_t num_splits, cudaStream_t stream);
 

@@ -244,3 +244,44 @@ def test_argument_errors_return_status():
     with pytest.raises(pkv.PkvError):  # workspace missing for a split call
         pkv.paged_attention(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], 1,
                             w.scale, kv_blocks_per_split=1, workspace=None)
+
+
+@pytest.mark.parametrize("q_len", [16, 17, 32])
+def test_tensor_core_chunks_ragged_with_nan_slots(q_len):
+    # q_len >= 16 runs the tcgen05 kernel: partial row tiles (17), two row
+    # tiles (32), unaligned histories, a context equal to q_len, NaN patterns
+    # in every slot no context covers, splits through the workspace
+    ctx = [q_len, q_len + 3, 64 + q_len, 100, 257, 1000 + q_len, 77]
+    w = W.build("tc", ctx, 200, q_len=q_len, seed=30 + q_len)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_append(kc, vc, w.slot_mapping, w.k_new, w.v_new)
+    used = np.zeros((w.num_blocks, 16), bool)
+    for r, c in enumerate(ctx):
+        for t in range(c):
+            used[w.block_tables[r, t // 16], t % 16] = True
+    kc.transpose(0, 2, 1, 3)[~used] = NAN_BF16
+    vc.transpose(0, 2, 1, 3)[~used] = NAN_BF16
+    w2 = W.Workload(**{**w.__dict__, "k_cache": kc, "v_cache": vc})
+    ref = oracle_ref(w2, append=False)
+    for bps in (1, 3, 0, 1000):
+        out, _ = run_gpu(w2, bps=bps, append=False)
+        assert_close(bf16_to_f64(out), ref, what=f"tc q_len={q_len} bps={bps}")
+
+
+def test_tensor_core_chunk_peaky_logits_rescale():
+    # Large logits make the running max jump between tiles, exercising the
+    # lazy O rescale in tensor memory.  This is outside the N(0,1) workloads:
+    # with a near one-hot softmax the tensor-core path's BF16 weights P
+    # (relative rounding <= 2^-9 each) move the output by up to
+    # 2^-9 * max|v - out| <= 2^-8 * max|V|, plus the BF16 rounding of the
+    # output itself (<= 2^-9 * max|out|), so the max-abs bound is derived from
+    # that instead of the 1e-2 used for N(0,1) inputs.
+    w = W.build("tcpeaky", [600, 900, 40], 200, q_len=16, seed=40)
+    qf = (w.q.astype(np.uint32) << 16).view(np.float32) * 12.0
+    w.q = W.bf16_bits(qf)
+    ref = oracle_ref(w)
+    vmax = float(np.abs((w.v_cache.astype(np.uint32) << 16).view(np.float32)).max())
+    bound = 2.0 ** -8 * vmax + 2.0 ** -9 * float(np.abs(ref).max())
+    for bps in (2, 1000):
+        out, _ = run_gpu(w, bps=bps)
+        assert_close(bf16_to_f64(out), ref, max_abs=bound, what=f"tc peaky bps={bps}")
