@@ -11,21 +11,22 @@
 // tile), so S = Q K^T and O = P V run as tcgen05.mma with FP32 accumulators in
 // tensor memory, and softmax runs in FP32 on the CUDA cores in between.
 //
-// CTA = 6 warps, one (request, row tile, split, KV head):
+// CTA = 6 warps, one (request, row tile, split, KV head); 2 CTAs per SM:
 //   warp 0  : TMA producer.  A KV tile is 4 blocks (64 tokens): for each block
 //             two 16x64 boxes of K and two of V (128-byte swizzle) land in a
-//             2-stage ring; blocks past the range are fetched at an
+//             3-stage ring; blocks past the range are fetched at an
 //             out-of-range row so TMA fills them with zeros.
-//   warp 1  : MMA issuer (one thread).  S_j = Q K_j^T (M 64, N 64, 8 k-steps)
-//             into a double-buffered TMEM S; O += P_j V_j (M 64, N 128, 4
-//             k-steps) into TMEM O.  S_{j+1} is issued before waiting for P_j
+//   warp 1  : MMA issuer (one thread).  S_j = Q K_j^T (M 64, N 64, 8 k-steps,
+//             Q and K from shared memory) into a double-buffered TMEM S;
+//             O += P_j V_j (M 64, N 128, 4 k-steps, P from TMEM, V from shared
+//             memory) into TMEM O.  S_{j+1} is issued before waiting for P_j
 //             so QK^T overlaps the softmax.
 //   warps 2-5: softmax.  Thread = one row (TMEM lanes 0-15 of each 32-lane
-//             sub-partition hold the M=64 accumulator).  Scores are masked
+//             sub-partition hold an M=64 accumulator).  Scores are masked
 //             (causal and context), scaled into base 2, exponentiated against
 //             a lazily updated row max (O in TMEM is rescaled only when a row
-//             max grows by more than 2^8), written as BF16 P into a 128-byte
-//             swizzled shared tile, and handed to the MMA warp.
+//             max grows by more than 2^8), and written back as BF16 P over the
+//             S buffer they came from, the A operand of the next PV MMA.
 //   epilogue: O / l to BF16 (one split) or FP32 + lse (split-KV partials).
 #include <cmath>
 #include <cstring>
@@ -38,26 +39,30 @@
 namespace pkv {
 namespace {
 
+// KV ring depth (32 KiB per stage): with P kept in tensor memory, 16 KiB of
+// Q plus 3 stages fit twice into an SM's shared memory.
+#ifndef PKV_TC_STAGES
+#define PKV_TC_STAGES 3
+#endif
 constexpr int kTcThreads = 192;
-constexpr int kTcStages = 2;
+constexpr int kTcStages = PKV_TC_STAGES;
+constexpr int kTcMinCtas = kTcStages <= 3 ? 2 : 1;
 constexpr int kTileBlocks = 4;                        // KV blocks per tile
 constexpr int kTileTokens = kTileBlocks * kBlockSize;  // 64
 constexpr int kRows = 64;                             // 16 positions x 4 heads
 constexpr int kQBytes = kRows * kHeadDim * 2;         // 16 KiB
-constexpr int kPBytes = kRows * kTileTokens * 2;      // 8 KiB
 constexpr int kHalfBytes = kTileTokens * 128;         // 64 tokens x 64 dims = 8 KiB
 constexpr int kStageBytesTc = 4 * kHalfBytes;         // K lo/hi, V lo/hi: 32 KiB
 constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffKV = kOffP + 2 * kPBytes;
+constexpr int kOffKV = kOffQ + kQBytes;
 constexpr int kOffBar = kOffKV + kTcStages * kStageBytesTc;
 constexpr int kSmemTc = kOffBar + 256;
-constexpr uint32_t kTmemCols = 256;  // S0 [0,64), S1 [64,128), O [128,256)
+constexpr uint32_t kTmemCols = 256;  // S/P buffer 0 [0,64), buffer 1 [64,128), O [128,256)
 constexpr uint32_t kColO = 128;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: weights stay below 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 
-static_assert(kSmemTc <= 113 * 1024, "two CTAs per SM");
+static_assert(kSmemTc <= (kTcMinCtas == 2 ? 113 : 227) * 1024, "shared memory per CTA");
 
 struct TcBars {
   uint64_t kv_full[kTcStages];
@@ -70,7 +75,7 @@ struct TcBars {
 static_assert(sizeof(TcBars) <= 256, "barrier area");
 
 template <bool kSplit>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
     paged_chunk_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                           const ChunkArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -219,7 +224,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const int st = j % kTcStages;
         const int sb = j & 1;
         if (!mbar_wait(&bars->kv_full[st], (j / kTcStages) & 1)) return false;
-        if (j >= 2 && !mbar_wait(&bars->p_full[sb], ((j - 2) >> 1) & 1)) return false;
+        // buffer sb holds P_{j-2} until PV_{j-2} has consumed it
+        if (j >= 2 && !mbar_wait(&bars->o_done[sb], ((j - 2) >> 1) & 1)) return false;
         tc::fence_after_sync();
         const uint32_t kst = sbase + kOffKV + st * kStageBytesTc;
 #pragma unroll
@@ -238,12 +244,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (!ok) break;
         tc::fence_after_sync();
         const int st = j % kTcStages;
-        const uint32_t pst = sbase + kOffP + (j & 1) * kPBytes;
+        const uint32_t ptm = tmem + (j & 1) * 64;  // P_j: 64 BF16 per row packed in 32 columns
         const uint32_t vst = sbase + kOffKV + st * kStageBytesTc + 2 * kHalfBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_bf16(tmem + kColO, tc::smem_desc(pst + 32 * kk, 16, 1024),
-                       tc::smem_desc(vst + 2048 * kk, kHalfBytes, 1024), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_bf16_tmem_a(tmem + kColO, ptm + 8 * kk, tc::smem_desc(vst + 2048 * kk, kHalfBytes, 1024), kIdO,
+                              (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc::commit(&bars->o_done[j & 1]);
         tc::commit(&bars->kv_empty[st]);
@@ -271,11 +277,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tc::tmem_ld32(tmem + lane_off + sb * 64 + 32, s + 32);
       tc::tmem_wait_ld();
       const int tok0 = (b0 + j * kTileBlocks) * kBlockSize;
-      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTileTokens; ++c) {
-        s[c] = (tok0 + c < n_vis_row) ? s[c] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+      for (int c = 0; c < kTileTokens; ++c) s[c] = (tok0 + c < n_vis_row) ? s[c] * a.scale_log2 : -INFINITY;
+      float mx;
+      {
+        float t8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float u = fmaxf(fmaxf(s[e], s[e + 8]), fmaxf(s[e + 16], s[e + 24]));
+          float v = fmaxf(fmaxf(s[e + 32], s[e + 40]), fmaxf(s[e + 48], s[e + 56]));
+          t8[e] = fmaxf(u, v);
+        }
+        mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
       }
       const bool grow = mx > m_stale + kRescaleThreshold;  // also true the first time a row sees a key
       const float m_new = grow ? mx : m_stale;
@@ -298,27 +311,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       l *= alpha;
       m_stale = m_new;
       const float m_use = (m_stale == -INFINITY) ? 0.f : m_stale;
-      // P buffer sb was last read by PV_{j-2}
-      if (j >= 2) ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars->o_done[sb], ((j - 2) >> 1) & 1));
-      uint8_t* prow = smem + kOffP + sb * kPBytes;
-      float rs = 0.f;
+      // P_j overwrites the S_j buffer it came from: 2 BF16 per 32-bit column
+      float pk[32];
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = exp2_approx(s[cc * 8 + e] - m_use);
-          rs += p[e];
-        }
-        if (lane < 16) {
-          uint4 w;
-          w.x = pack_bf16x2(p[0], p[1]);
-          w.y = pack_bf16x2(p[2], p[3]);
-          w.z = pack_bf16x2(p[4], p[5]);
-          w.w = pack_bf16x2(p[6], p[7]);
-          *reinterpret_cast<uint4*>(prow + tc::sw128_offset(row, cc * 8)) = w;
-        }
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = exp2_approx(s[2 * c] - m_use);
+        const float p1 = exp2_approx(s[2 * c + 1] - m_use);
+        rs8[c & 7] += p0 + p1;
+        pk[c] = __uint_as_float(pack_bf16x2(p0, p1));
       }
+      tc::tmem_st32(tmem + lane_off + sb * 64, pk);
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       l += rs;
       // slots past the request's data in its last block may hold anything: zero those V rows
       const int tile_end = tok0 + kTileTokens;
@@ -333,7 +337,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           *reinterpret_cast<uint4*>(vt + (ch >> 3) * kHalfBytes + tk * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_st();
+      tc::fence_proxy_async_smem();  // zeroed V rows, if any, before the PV MMA reads them
       tc::fence_before_sync();
       mbar_arrive(&bars->p_full[sb]);
     }
