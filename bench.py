@@ -219,6 +219,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--kv-blocks-per-split", type=int, default=0)
     ap.add_argument("--graph", action="store_true", help="replay each step as one CUDA graph")
+    ap.add_argument("--prefix-blocks-per-split", type=int, default=0, help="cascade prefix pass split (0 = plan)")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="shared-prefix workloads: plain paged attention instead of the cascade call")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -281,6 +284,18 @@ def main():
     kp0, vp0 = k_pool.data_ptr(), v_pool.data_ptr()
     q_stride, kn_stride = b * ql * hq * d * 2, t_tok * hkv * d * 2
     launches_per_layer = 1 + 1 + (1 if splits > 1 else 0)
+    # shared prefixes: the caller states the groups and the cascade call reads each prefix once per group
+    gs_h, gb_h, sp_h = W.prefix_groups(w)
+    cascade = (not args.no_cascade) and gs_h.shape[0] > 0 and ql == 1
+    if cascade:
+        maxp = int(gb_h.max())
+        pbps, sbps = pkv.cascade_plan(b, hkv, gs_h.shape[0], maxp, maxb)
+        pbps = args.prefix_blocks_per_split or pbps
+        cws = torch.empty(max(256, pkv.cascade_workspace_size(b, hq, maxp, maxb, pbps, sbps)), dtype=torch.uint8,
+                          device=dev)
+        gs_d, gb_d, sp_d = (torch.from_numpy(x).to(dev) for x in (gs_h, gb_h, sp_h))
+        splits = -(-maxp // pbps) + -(-maxb // sbps)
+        launches_per_layer = 1 + 3
 
     def check(st, what):
         if st != 0:
@@ -292,10 +307,17 @@ def main():
               "kv_append")
         if ev is not None:
             ev[0].record(stream)
-        check(lib.pkv_paged_attention(out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride,
-                                      kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc),
-                                      tables.data_ptr(), maxb, ctx.data_ptr(), b, ql, hq, w.scale, bps,
-                                      ws.data_ptr(), ws.numel(), sp), "paged_attention")
+        if cascade:
+            check(lib.pkv_paged_attention_cascade(
+                out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride, kp0 + l * pool_stride,
+                vp0 + l * pool_stride, ctypes.byref(desc), tables.data_ptr(), maxb, ctx.data_ptr(), b, hq, w.scale,
+                gs_d.data_ptr(), gb_d.data_ptr(), sp_d.data_ptr(), gs_h.shape[0], maxp, pbps, sbps, cws.data_ptr(),
+                cws.numel(), sp), "paged_attention_cascade")
+        else:
+            check(lib.pkv_paged_attention(out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride,
+                                          kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc),
+                                          tables.data_ptr(), maxb, ctx.data_ptr(), b, ql, hq, w.scale, bps,
+                                          ws.data_ptr(), ws.numel(), sp), "paged_attention")
         if ev is not None:
             ev[1].record(stream)
 
@@ -360,8 +382,12 @@ def main():
                 dst.copy_(src, non_blocking=True)
             for l in range(layers):
                 pkv.kv_append(k_pool[l], v_pool[l], slots, kn[l], vn[l])
-                pkv.paged_attention(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, ql, w.scale,
-                                    kv_blocks_per_split=bps, workspace=ws)
+                if cascade:
+                    pkv.paged_attention_cascade(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, w.scale, gs_d, gb_d,
+                                                sp_d, maxp, cws, pbps, sbps)
+                else:
+                    pkv.paged_attention(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, ql, w.scale,
+                                        kv_blocks_per_split=bps, workspace=ws)
             p_out.copy_(out, non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
@@ -411,6 +437,8 @@ def main():
                    "layers": layers, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16,
                    "ctx_min": int(w.context_lens.min()), "ctx_max": int(w.context_lens.max()),
                    "kv_blocks_per_split": bps, "splits": splits, "cuda_graph": bool(graph is not None),
+                   "cascade": ({"groups": int(gs_h.shape[0]), "prefix_blocks": maxp, "prefix_blocks_per_split": pbps,
+                                "suffix_blocks_per_split": sbps} if cascade else None),
                    "l2": "inputs larger than L2: one KV pool per layer, %.1f GB total" % (
                        2 * k_pool.numel() * 2 / 1e9),
                    "parallelism": f"replicas x{world}"},
@@ -420,7 +448,10 @@ def main():
         "bytes_per_step": int(step_bytes),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
-                     "kernel": "paged_attention call (decode%s)" % (" + combine" if splits > 1 else ""),
+                     "kernel": ("paged_attention_cascade call (prefix tensor-core pass + suffix decode + combine)"
+                                if cascade else "paged_attention call (%s%s)" % (
+                                    "tensor-core chunk" if ql >= 16 else "decode",
+                                    " + combine" if (splits > 8 or (ql >= 16 and splits > 1)) else "")),
                      "algorithmic_bytes_per_launch": int(attn_b)},
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "cpu_baseline": cpu, "e2e": e2e,

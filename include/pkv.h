@@ -157,6 +157,49 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
                                int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/*
+ * Cascade decode: requests whose block tables begin with the same physical
+ * blocks (a common prefix stored once, §8.3.1 worked example and Fig. 8-13;
+ * §8.3.2's shared-prefix batch) read that prefix together.  For each group of
+ * up to 16 sharers, one tensor-core pass contracts the 16 x 4 query rows of
+ * a KV head against the prefix tiles once; each request's private suffix goes
+ * through the decode kernel; the partial results are merged by the
+ * log-sum-exp identity.  The result equals pkv_paged_attention's (q_len 1).
+ *
+ *   group_seqs        : device int32 [num_groups][16]: member request indices,
+ *                       -1 for unused places (member 0 must be valid).
+ *   group_blocks      : device int32 [num_groups]: P_g, the number of leading
+ *                       logical blocks every member of group g maps to the
+ *                       same physical blocks (read through member 0's row).
+ *   seq_prefix_blocks : device int32 [num_seqs]: P_g of the group holding
+ *                       request r, 0 for a request in no group.  A request
+ *                       belongs to at most one group.
+ *   num_groups        : >= 0 (0: every request is a plain decode).
+ *   max_prefix_blocks : host upper bound of every P_g (sizes the prefix split).
+ *   prefix_blocks_per_split, suffix_blocks_per_split : 0 = pkv_cascade_plan.
+ *   workspace         : >= pkv_cascade_workspace_size(...) bytes, 256-aligned.
+ * Every other argument is as for pkv_paged_attention with q_len = 1.  A member
+ * whose context is shorter than P_g*16 tokens still gets the exact result (its
+ * prefix rows are masked at its own context), it only saves nothing.
+ */
+void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups, int32_t max_prefix_blocks,
+                      int32_t max_blocks_per_seq, int32_t sm_count, int32_t* prefix_blocks_per_split,
+                      int32_t* suffix_blocks_per_split);
+
+size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_prefix_blocks,
+                                  int32_t max_blocks_per_seq, int32_t prefix_blocks_per_split,
+                                  int32_t suffix_blocks_per_split);
+
+pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const pkv_cache_desc* cache, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t num_seqs, int32_t num_q_heads, float scale,
+                                       const int32_t* group_seqs, const int32_t* group_blocks,
+                                       const int32_t* seq_prefix_blocks, int32_t num_groups,
+                                       int32_t max_prefix_blocks, int32_t prefix_blocks_per_split,
+                                       int32_t suffix_blocks_per_split, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
 /* Bytes of the scratch array compiled into libpkv for
  * pkv_paged_attention_static_workspace (held on every GPU that loads the
  * library, until the process exits). */

@@ -20,7 +20,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "PkvError", "kv_append", "paged_attention", "attn_combine", "workspace_size",
+    "PkvError", "kv_append", "paged_attention", "paged_attention_cascade", "cascade_plan",
+    "cascade_workspace_size", "attn_combine", "workspace_size",
     "choose_kv_blocks_per_split", "get_device_error", "library_path", "lib", "DEVERR_BLOCK_ID",
     "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT",
 ]
@@ -61,6 +62,13 @@ def _load():
     lib.pkv_paged_attention.restype = ctypes.c_int
     lib.pkv_attn_combine.argtypes = [p, p, p, p, i32, i32, i32, p]
     lib.pkv_attn_combine.restype = ctypes.c_int
+    lib.pkv_cascade_plan.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.pkv_cascade_plan.restype = None
+    lib.pkv_cascade_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.pkv_cascade_workspace_size.restype = sz
+    lib.pkv_paged_attention_cascade.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32, f32,
+                                                p, p, p, i32, i32, i32, i32, p, sz, p]
+    lib.pkv_paged_attention_cascade.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.pkv_get_device_error.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -172,6 +180,52 @@ def paged_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v
                                     ctypes.byref(desc), block_tables.data_ptr(), maxb, context_lens.data_ptr(),
                                     b, q_len, hq, float(scale), bps, ws_ptr, ws_bytes, _stream_ptr(stream)),
            "pkv_paged_attention")
+
+
+def cascade_plan(num_seqs: int, num_kv_heads: int, num_groups: int, max_prefix_blocks: int,
+                 max_blocks_per_seq: int, sm_count: int = 0):
+    """(prefix_blocks_per_split, suffix_blocks_per_split) the cascade call would choose."""
+    pb, sb = ctypes.c_int32(0), ctypes.c_int32(0)
+    _lib.pkv_cascade_plan(num_seqs, num_kv_heads, num_groups, max_prefix_blocks, max_blocks_per_seq, sm_count,
+                          ctypes.byref(pb), ctypes.byref(sb))
+    return int(pb.value), int(sb.value)
+
+
+def cascade_workspace_size(num_seqs: int, num_q_heads: int, max_prefix_blocks: int, max_blocks_per_seq: int,
+                           prefix_blocks_per_split: int, suffix_blocks_per_split: int) -> int:
+    return int(_lib.pkv_cascade_workspace_size(num_seqs, num_q_heads, max_prefix_blocks, max_blocks_per_seq,
+                                               prefix_blocks_per_split, suffix_blocks_per_split))
+
+
+def paged_attention_cascade(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                            group_seqs: torch.Tensor, group_blocks: torch.Tensor, seq_prefix_blocks: torch.Tensor,
+                            max_prefix_blocks: int, workspace: torch.Tensor, prefix_blocks_per_split: int = 0,
+                            suffix_blocks_per_split: int = 0, stream=None) -> None:
+    """Decode attention (q_len 1) with shared prefixes contracted once per group of <= 16 sharers.
+
+    group_seqs int32 [G][16] (-1 = unused), group_blocks int32 [G], seq_prefix_blocks int32 [B];
+    workspace >= cascade_workspace_size(...) bytes."""
+    _bf16(out, "out"), _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    for t, n in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                 (seq_prefix_blocks, "seq_prefix_blocks")):
+        _i32(t, n)
+    b = context_lens.numel()
+    if q.dim() != 4 or q.shape[0] != b or q.shape[1] != 1 or out.shape != q.shape:
+        raise ValueError("q/out must be [num_seqs][1][num_q_heads][head_dim]")
+    g = group_seqs.shape[0] if group_seqs is not None else 0
+    if g:
+        _i32(group_seqs, "group_seqs"), _i32(group_blocks, "group_blocks")
+        if group_seqs.dim() != 2 or group_seqs.shape[1] != 16 or group_blocks.numel() != g:
+            raise ValueError("group_seqs must be [num_groups][16] and group_blocks [num_groups]")
+    desc = _desc(k_cache)
+    ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(_lib.pkv_paged_attention_cascade(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), b, q.shape[2], float(scale),
+        group_seqs.data_ptr() if g else 0, group_blocks.data_ptr() if g else 0, seq_prefix_blocks.data_ptr(), g,
+        int(max_prefix_blocks), int(prefix_blocks_per_split), int(suffix_blocks_per_split), ws_ptr, ws_bytes,
+        _stream_ptr(stream)), "pkv_paged_attention_cascade")
 
 
 def attn_combine(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.Tensor,

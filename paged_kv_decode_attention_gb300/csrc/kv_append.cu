@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
                                                         const uint4* __restrict__ k_new,
                                                         const uint4* __restrict__ v_new, int64_t total,
                                                         unsigned int* err) {
+  pdl_wait();  // new K/V and slots may come from the previous grid
+  pdl_trigger();
   // item = ((t * 2 + which) * Hkv + h) * 16 + chunk
   for (int64_t item = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; item < total;
        item += (int64_t)gridDim.x * blockDim.x) {
@@ -58,11 +60,10 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, int32_t num_blocks, i
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 65536) blocks = 65536;
-  kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-      static_cast<int64_t>(num_blocks) * kBlockSize, num_kv_heads, slot_mapping,
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), total, err);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, 1,
+                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                    static_cast<int64_t>(num_blocks) * kBlockSize, num_kv_heads, slot_mapping,
+                    static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), total, err);
 }
 
 }  // namespace pkv

@@ -75,30 +75,45 @@ struct TcBars {
 static_assert(sizeof(TcBars) <= 256, "barrier area");
 
 template <bool kSplit>
-__global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
-    paged_chunk_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
-                          const ChunkArgs a) {
+__device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                                    const ChunkArgs& a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   TcBars* bars = reinterpret_cast<TcBars*>(smem + kOffBar);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int n_rt = (a.q_len + 15) / 16;   // row tiles per request
-  const int r = blockIdx.x / n_rt;
-  const int rt = blockIdx.x - r * n_rt;
+  const bool cascade = a.group_seqs != nullptr;
+  const int n_rt = (a.q_len + 15) / 16;  // row tiles per request (chunk mode)
   const int split = blockIdx.y;
   const int kvh = blockIdx.z;
   const int hq = a.num_kv_heads * kGroup;
-  const int ctx = a.context_lens[r];
   const int cap = a.max_blocks * kBlockSize;
-  if (ctx > cap && threadIdx.x == 0 && split == 0 && kvh == 0 && rt == 0) report(a.err, PKV_DEVERR_CONTEXT);
-  // last position of this row tile and the keys it sees (the most of any row here)
-  const int ip_last = min(a.q_len - 1, rt * 16 + 15);
-  int n_vis_cta = ctx - a.q_len + 1 + ip_last;
-  if (ctx <= 0 || n_vis_cta < 0) n_vis_cta = 0;
-  n_vis_cta = min(n_vis_cta, cap);
-  const int ctx_keys = min(max(ctx, 0), cap);  // keys that hold data (the rest of a block may be garbage)
-  const int nb = (n_vis_cta + kBlockSize - 1) / kBlockSize;
+  // Row m of the 64-row tile is (request row_req(m), query position row_pos(m), head m % 4).
+  //   chunk mode  : one request, positions rt*16 + m/4 (q_len tokens, causal);
+  //   cascade mode: member m/4 of prefix group blockIdx.x, its single query.
+  int r = 0, rt = 0, table_row = 0, nb = 0, ctx_keys = 0;
+  const int32_t* members = nullptr;
+  if (cascade) {
+    members = a.group_seqs + static_cast<int64_t>(blockIdx.x) * kCascadeGroup;
+    table_row = members[0];
+    nb = table_row >= 0 ? min(a.group_blocks[blockIdx.x], a.max_blocks) : 0;
+    ctx_keys = nb * kBlockSize;  // prefix blocks are full: no garbage slots
+  } else {
+    r = blockIdx.x / n_rt;
+    rt = blockIdx.x - r * n_rt;
+    table_row = r;
+    const int ctx = a.context_lens[r];
+    if (ctx > cap && threadIdx.x == 0 && split == 0 && kvh == 0 && rt == 0) report(a.err, PKV_DEVERR_CONTEXT);
+    // the last position of this row tile sees the most keys
+    const int ip_last = min(a.q_len - 1, rt * 16 + 15);
+    int n_vis_cta = ctx - a.q_len + 1 + ip_last;
+    if (ctx <= 0 || n_vis_cta < 0) n_vis_cta = 0;
+    n_vis_cta = min(n_vis_cta, cap);
+    nb = (n_vis_cta + kBlockSize - 1) / kBlockSize;
+    ctx_keys = min(max(ctx, 0), cap);  // keys holding data (the rest of the last block may be garbage)
+  }
+  auto row_req = [&](int m) -> int { return cascade ? members[m >> 2] : r; };
+  auto row_pos = [&](int m) -> int { return cascade ? 0 : rt * 16 + (m >> 2); };
   const int b0 = split * a.blocks_per_split;
   const int b1 = min(nb, b0 + a.blocks_per_split);
   const int n_tiles = (b1 - b0 + kTileBlocks - 1) / kTileBlocks;
@@ -106,15 +121,17 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
   // rows handled by softmax threads: warp w >= 2 owns TMEM sub-partition w % 4
   const int quad = warp & 3;
   const int row = quad * 16 + lane;  // meaningful for lane < 16
-  const int ip = rt * 16 + (row >> 2);
+  const int rq = (warp >= 2 && lane < 16) ? row_req(row) : -1;
+  const int ip = row_pos(row);
   const int g = row & 3;
-  const bool row_valid = warp >= 2 && lane < 16 && ip < a.q_len;
-  const int64_t orow = (static_cast<int64_t>(r) * a.q_len + ip) * hq + kvh * kGroup + g;
+  const bool row_valid = warp >= 2 && lane < 16 && rq >= 0 && ip < a.q_len;
+  const int64_t orow = (static_cast<int64_t>(rq) * a.q_len + ip) * hq + kvh * kGroup + g;
+  const int64_t slot = orow * a.part_slots + a.part_slot0 + split;
 
   if (n_tiles <= 0) {
     if (row_valid) {
       if constexpr (kSplit) {
-        a.part_lse[orow * a.num_splits + split] = -INFINITY;
+        a.part_lse[slot] = -INFINITY;
       } else {
         uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim);
 #pragma unroll
@@ -152,11 +169,12 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
     for (int idx = t; idx < kRows * 16; idx += 128) {
       const int m = idx >> 4;
       const int ch = idx & 15;  // 16-byte chunk of the row
-      const int ipm = rt * 16 + (m >> 2);
+      const int ipm = row_pos(m);
+      const int rm = row_req(m);
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (ipm < a.q_len)
+      if (rm >= 0 && ipm < a.q_len)
         v = *reinterpret_cast<const uint4*>(
-            qbase + ((static_cast<int64_t>(r) * a.q_len + ipm) * hq + kvh * kGroup + (m & 3)) * kHeadDim + ch * 8);
+            qbase + ((static_cast<int64_t>(rm) * a.q_len + ipm) * hq + kvh * kGroup + (m & 3)) * kHeadDim + ch * 8);
       const int half = ch >> 3;
       *reinterpret_cast<uint4*>(smem + kOffQ + half * 8192 + tc::sw128_offset(m, (ch & 7) * 8)) = v;
     }
@@ -172,7 +190,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
   if (warp == 0) {
     // ---------------------------- TMA producer ----------------------------
     const uint64_t policy = l2_policy_evict_first();
-    const int32_t* table = a.block_tables + static_cast<int64_t>(r) * a.max_blocks;
+    const int32_t* table = a.block_tables + static_cast<int64_t>(table_row) * a.max_blocks;
     const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;  // first row past the pool
     const int n_blocks = b1 - b0;
     for (int base = 0; base < n_tiles * kTileBlocks && ok; base += 32) {
@@ -262,7 +280,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     // keys this row may see inside this split: causal limit, context, and the
     // split's own block range (the tail tile's extra blocks arrive zero-filled)
-    const int n_vis_row = row_valid ? min(min(max(ctx - a.q_len + 1 + ip, 0), cap), b1 * kBlockSize) : 0;
+    int n_vis_row = 0;
+    if (row_valid) {
+      const int ctx_r = a.context_lens[rq];
+      n_vis_row = min(min(max(ctx_r - a.q_len + 1 + ip, 0), cap), b1 * kBlockSize);
+    }
     float m_stale = -INFINITY;  // max the weights are taken against (lags the true max by < 2^8)
     float l = 0.f;
     for (int j = 0; j < n_tiles && ok; ++j) {
@@ -355,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
       tc::tmem_wait_ld();
       if (row_valid && ok) {
         if constexpr (kSplit) {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + (orow * a.num_splits + split) * kHeadDim + 32 * cc);
+          float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kHeadDim + 32 * cc);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
@@ -374,7 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
       }
     }
     if constexpr (kSplit) {
-      if (row_valid && ok) a.part_lse[orow * a.num_splits + split] = lse;
+      if (row_valid && ok) a.part_lse[slot] = lse;
     }
   }
 
@@ -384,6 +406,15 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+template <bool kSplit>
+__global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
+    paged_chunk_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                          const ChunkArgs a) {
+  pdl_wait();  // inputs come from earlier grids in the stream
+  pdl_trigger();
+  paged_chunk_tc_body<kSplit>(k_map, v_map, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -437,24 +468,21 @@ cudaError_t allow_smem_tc() {
 
 }  // namespace
 
-cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, cudaStream_t stream) {
+cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, int32_t grid_x, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;
   if (rows + kBlockSize >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
   CUtensorMap kmap, vmap;
   if (!make_pool_map(&kmap, a.k_cache, rows) || !make_pool_map(&vmap, a.v_cache, rows)) return cudaErrorInvalidValue;
-  const int n_rt = (a.q_len + 15) / 16;
-  const dim3 grid(static_cast<unsigned>(a.num_seqs * n_rt), static_cast<unsigned>(a.num_splits),
+  const dim3 grid(static_cast<unsigned>(grid_x), static_cast<unsigned>(a.num_splits),
                   static_cast<unsigned>(a.num_kv_heads));
   if (grid.x == 0) return cudaSuccess;
   cudaError_t e;
-  if (a.num_splits > 1) {
+  if (a.part_o != nullptr) {  // partials to the workspace (splits, or a cascade prefix pass)
     if ((e = allow_smem_tc<true>()) != cudaSuccess) return e;
-    paged_chunk_tc_kernel<true><<<grid, kTcThreads, kSmemTc, stream>>>(kmap, vmap, a);
-  } else {
-    if ((e = allow_smem_tc<false>()) != cudaSuccess) return e;
-    paged_chunk_tc_kernel<false><<<grid, kTcThreads, kSmemTc, stream>>>(kmap, vmap, a);
+    return launch_pdl(paged_chunk_tc_kernel<true>, grid, dim3(kTcThreads), kSmemTc, stream, 1, kmap, vmap, a);
   }
-  return cudaGetLastError();
+  if ((e = allow_smem_tc<false>()) != cudaSuccess) return e;
+  return launch_pdl(paged_chunk_tc_kernel<false>, grid, dim3(kTcThreads), kSmemTc, stream, 1, kmap, vmap, a);
 }
 
 }  // namespace pkv

@@ -98,7 +98,7 @@ __device__ __forceinline__ void unpack8x2(const uint4 v, float2* f) {
 }
 
 template <int NS, SplitMode kMode>
-__global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) paged_decode_kernel(const DecodeArgs a) {
+__device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
   using L = DecodeSmem<NS>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) paged_decode_ke
   }
   if (ctx <= 0 || n_vis < 0) n_vis = 0;
   const int nb = (n_vis + kBlockSize - 1) / kBlockSize;
-  const int b0 = split * a.blocks_per_split;
+  const int start = a.seq_start_block ? a.seq_start_block[r] : 0;  // blocks before it are reduced elsewhere
+  const int b0 = start + split * a.blocks_per_split;
   const int b1 = min(nb, b0 + a.blocks_per_split);
   const int64_t qrow0 = static_cast<int64_t>(vrow) * hq + kvh * kGroup;  // (r, i, first head of group)
   const bool empty = b0 >= b1;
@@ -140,7 +141,11 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) paged_decode_ke
             make_uint4(0, 0, 0, 0);
       return;
     } else if constexpr (kMode == SplitMode::kWorkspace) {
-      if (threadIdx.x < kGroup) a.part_lse[(qrow0 + threadIdx.x) * a.num_splits + split] = -INFINITY;
+      if (threadIdx.x < kGroup) {
+        a.part_lse[(qrow0 + threadIdx.x) * a.part_slots + a.part_slot0 + split] = -INFINITY;
+        if (split == 0 && start == 0)
+          for (int sl = 0; sl < a.part_slot0; ++sl) a.part_lse[(qrow0 + threadIdx.x) * a.part_slots + sl] = -INFINITY;
+      }
       return;
     } else {
       // cluster mode: an empty partial still takes part in the cluster merge
@@ -395,10 +400,13 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) paged_decode_ke
           packed.y = pack_bf16x2(o[2], o[3]);
           *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim + d0) = packed;
         } else {
-          *reinterpret_cast<float4*>(a.part_o + (orow * a.num_splits + split) * kHeadDim + d0) =
-              make_float4(o[0], o[1], o[2], o[3]);
-          if (lane == 0)
-            a.part_lse[orow * a.num_splits + split] = (mx == -INFINITY) ? -INFINITY : (mx + log2f(sum)) * kLn2;
+          const int64_t slot = orow * a.part_slots + a.part_slot0 + split;
+          *reinterpret_cast<float4*>(a.part_o + slot * kHeadDim + d0) = make_float4(o[0], o[1], o[2], o[3]);
+          if (lane == 0) {
+            a.part_lse[slot] = (mx == -INFINITY) ? -INFINITY : (mx + log2f(sum)) * kLn2;
+            if (split == 0 && start == 0)
+              for (int sl = 0; sl < a.part_slot0; ++sl) a.part_lse[orow * a.part_slots + sl] = -INFINITY;
+          }
         }
       }
     }
@@ -442,6 +450,14 @@ __global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) paged_decode_ke
   }
 }
 
+template <int NS, SplitMode kMode>
+__global__ void __launch_bounds__(kThreads, PKV_DECODE_MIN_CTAS) paged_decode_kernel(const DecodeArgs a) {
+  if (!a.overlap_previous) pdl_wait();  // inputs come from earlier grids in the stream
+  pdl_trigger();
+  paged_decode_body<NS, kMode>(a);
+  if (a.overlap_previous) pdl_wait();  // complete only after the grid it overlapped
+}
+
 constexpr int kStages = PKV_DECODE_STAGES;
 
 // Opt the kernel in to more than 48 KiB of dynamic shared memory, once per
@@ -472,31 +488,31 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.num_splits == 1) {
     cudaError_t e = allow_smem<SplitMode::kDirect>(L::kBytes);
     if (e != cudaSuccess) return e;
-    paged_decode_kernel<kStages, SplitMode::kDirect><<<grid, kThreads, L::kBytes, stream>>>(a);
-  } else if (a.part_o == nullptr) {
-    if (a.num_splits > kMaxClusterSplits) return cudaErrorInvalidValue;
-    cudaError_t e0 = allow_smem<SplitMode::kCluster>(L::kBytes);
-    if (e0 != cudaSuccess) return e0;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = L::kBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = static_cast<unsigned>(a.num_splits);
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<kStages, SplitMode::kCluster>, a);
-    if (e != cudaSuccess) return e;
-  } else {
-    cudaError_t e = allow_smem<SplitMode::kWorkspace>(L::kBytes);
-    if (e != cudaSuccess) return e;
-    paged_decode_kernel<kStages, SplitMode::kWorkspace><<<grid, kThreads, L::kBytes, stream>>>(a);
+    return launch_pdl(paged_decode_kernel<kStages, SplitMode::kDirect>, grid, dim3(kThreads), L::kBytes, stream, 1,
+                      a);
   }
-  return cudaGetLastError();
+  if (a.part_o == nullptr) {
+    if (a.num_splits > kMaxClusterSplits) return cudaErrorInvalidValue;
+    cudaError_t e = allow_smem<SplitMode::kCluster>(L::kBytes);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(paged_decode_kernel<kStages, SplitMode::kCluster>, grid, dim3(kThreads), L::kBytes, stream,
+                      static_cast<unsigned>(a.num_splits), a);
+  }
+  cudaError_t e = allow_smem<SplitMode::kWorkspace>(L::kBytes);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(paged_decode_kernel<kStages, SplitMode::kWorkspace>, grid, dim3(kThreads), L::kBytes, stream, 1,
+                    a);
+}
+
+cudaError_t launch_paged_decode_workspace(const DecodeArgs& a, cudaStream_t stream) {
+  using L = DecodeSmem<kStages>;
+  const dim3 grid(static_cast<unsigned>(a.num_seqs * a.q_len), static_cast<unsigned>(a.num_splits),
+                  static_cast<unsigned>(a.num_kv_heads));
+  if (grid.x == 0) return cudaSuccess;
+  cudaError_t e = allow_smem<SplitMode::kWorkspace>(L::kBytes);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(paged_decode_kernel<kStages, SplitMode::kWorkspace>, grid, dim3(kThreads), L::kBytes, stream, 1,
+                    a);
 }
 
 }  // namespace pkv

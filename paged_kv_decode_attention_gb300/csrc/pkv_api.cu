@@ -173,6 +173,9 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
   a.blocks_per_split = bps;
   a.num_splits = splits;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.part_slots = splits;
+  a.part_slot0 = 0;
+  const int32_t tc_grid_x = num_seqs * ((q_len + 15) / 16);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool tensor_cores = q_len >= kTcMinQLen;
@@ -184,14 +187,128 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
     a.part_o = static_cast<float*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                           align_up(rows * splits * kHeadDim * sizeof(float), 256));
-    if ((tensor_cores ? launch_paged_chunk_tc(a, s) : launch_paged_decode(a, s)) != cudaSuccess)
+    if ((tensor_cores ? launch_paged_chunk_tc(a, tc_grid_x, s) : launch_paged_decode(a, s)) != cudaSuccess)
       return PKV_ERR_CUDA;
     if (launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), splits, s) != cudaSuccess)
       return PKV_ERR_CUDA;
     return PKV_OK;
   }
-  return (tensor_cores ? launch_paged_chunk_tc(a, s) : launch_paged_decode(a, s)) == cudaSuccess ? PKV_OK
+  return (tensor_cores ? launch_paged_chunk_tc(a, tc_grid_x, s) : launch_paged_decode(a, s)) == cudaSuccess ? PKV_OK
                                                                                                  : PKV_ERR_CUDA;
+}
+
+void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups, int32_t max_prefix_blocks,
+                      int32_t max_blocks_per_seq, int32_t sm_count, int32_t* prefix_blocks_per_split,
+                      int32_t* suffix_blocks_per_split) {
+  if (sm_count <= 0) sm_count = device_sm_count();
+  const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
+  // prefix pass: enough (group, split, head) CTAs to fill the GPU, each at least one 64-token tile
+  int32_t pbps = max_prefix_blocks > 0 ? max_prefix_blocks : 1;
+  const int64_t prows = static_cast<int64_t>(num_groups > 0 ? num_groups : 1) * num_kv_heads;
+  if (max_prefix_blocks > 0 && prows < slots) {
+    const int64_t sp = (slots + prows - 1) / prows;
+    pbps = static_cast<int32_t>((max_prefix_blocks + sp - 1) / sp);
+    pbps = ((pbps + 3) / 4) * 4;  // whole 4-block tiles
+    if (pbps < 16) pbps = 16;
+  }
+  // suffix pass: the decode heuristic over the part of the longest table past
+  // the longest prefix
+  int32_t span = max_blocks_per_seq - (max_prefix_blocks > 0 ? max_prefix_blocks : 0);
+  int32_t sbps = pkv_choose_kv_blocks_per_split(num_seqs, num_kv_heads, 1, span > 0 ? span : 1, sm_count);
+  if (prefix_blocks_per_split) *prefix_blocks_per_split = pbps;
+  if (suffix_blocks_per_split) *suffix_blocks_per_split = sbps;
+}
+
+static int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_prefix_blocks,
+                                  int32_t max_blocks_per_seq, int32_t prefix_blocks_per_split,
+                                  int32_t suffix_blocks_per_split) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || prefix_blocks_per_split <= 0 ||
+      suffix_blocks_per_split <= 0)
+    return 0;
+  const size_t slots = static_cast<size_t>(max_prefix_blocks > 0 ? ceil_div(max_prefix_blocks, prefix_blocks_per_split) : 0) +
+                       ceil_div(max_blocks_per_seq, suffix_blocks_per_split);
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
+  return align_up(rows * slots * kHeadDim * sizeof(float), 256) + align_up(rows * slots * sizeof(float), 256);
+}
+
+pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const pkv_cache_desc* cache, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                       int32_t num_q_heads, float scale, const int32_t* group_seqs,
+                                       const int32_t* group_blocks, const int32_t* seq_prefix_blocks,
+                                       int32_t num_groups, int32_t max_prefix_blocks,
+                                       int32_t prefix_blocks_per_split, int32_t suffix_blocks_per_split,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_blocks_per_seq < 1 || num_groups < 0 || max_prefix_blocks < 0 ||
+      max_prefix_blocks > max_blocks_per_seq || prefix_blocks_per_split < 0 || suffix_blocks_per_split < 0)
+    return PKV_ERR_SHAPE;
+  if (num_q_heads != kGroup * cache->num_kv_heads) return PKV_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return PKV_ERR_SHAPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !seq_prefix_blocks) return PKV_ERR_NULL;
+  if (num_groups > 0 && (!group_seqs || !group_blocks)) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return PKV_ERR_UNSUPPORTED;
+  int32_t pbps = prefix_blocks_per_split, sbps = suffix_blocks_per_split;
+  if (pbps == 0 || sbps == 0) {
+    int32_t p0 = 0, s0 = 0;
+    pkv_cascade_plan(num_seqs, cache->num_kv_heads, num_groups, max_prefix_blocks, max_blocks_per_seq, 0, &p0, &s0);
+    if (pbps == 0) pbps = p0;
+    if (sbps == 0) sbps = s0;
+  }
+  const int32_t sp = (num_groups > 0 && max_prefix_blocks > 0) ? ceil_div(max_prefix_blocks, pbps) : 0;
+  const int32_t ss = ceil_div(max_blocks_per_seq, sbps);
+  if (sp > 65535 || ss > 65535) return PKV_ERR_UNSUPPORTED;
+  const size_t need = pkv_cascade_workspace_size(num_seqs, num_q_heads, max_prefix_blocks, max_blocks_per_seq, pbps, sbps);
+  if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
+  const int32_t slots = sp + ss;
+
+  DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.err = error_word();
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = cache->num_blocks;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.num_seqs = num_seqs;
+  a.q_len = 1;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        align_up(rows * slots * kHeadDim * sizeof(float), 256));
+  a.part_slots = slots;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (sp > 0) {
+    // shared prefixes: each group's members x 4 heads as one 64-row tensor-core tile
+    DecodeArgs p = a;
+    p.blocks_per_split = pbps;
+    p.num_splits = sp;
+    p.part_slot0 = 0;
+    p.group_seqs = group_seqs;
+    p.group_blocks = group_blocks;
+    if (launch_paged_chunk_tc(p, num_groups, s) != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  // private suffixes (and requests outside every group) on the decode kernel
+  a.blocks_per_split = sbps;
+  a.num_splits = ss;
+  a.part_slot0 = sp;
+  a.seq_start_block = seq_prefix_blocks;
+  a.overlap_previous = sp > 0 ? 1 : 0;  // the suffix pass runs beside the prefix pass
+  if (launch_paged_decode_workspace(a, s) != cudaSuccess) return PKV_ERR_CUDA;
+  if (launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), slots, s) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 pkv_status pkv_attn_combine(void* out, float* out_lse, const float* partial_o, const float* partial_lse,

@@ -160,6 +160,14 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
   return v;
 }
 
+// ---- programmatic dependent launch ----
+// Wait until the grids this one depends on have completed and their writes
+// are visible (a no-op when the launch had no programmatic dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid in the stream launch its CTAs (they still wait in
+// pdl_wait before touching this grid's results).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // BF16 pair to a float2 (element 0 in .x).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));

@@ -5,8 +5,41 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace pkv {
+
+// Launch `kernel` on `stream` with programmatic stream serialization: its
+// CTAs may be scheduled while the previous grid in the stream finishes; every
+// kernel of this library starts with pdl_wait() before reading any input, so
+// results are the same as with a plain launch.  cluster_y > 1 also groups
+// the grid's y dimension into thread-block clusters of that size.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       unsigned cluster_y, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_y > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = cluster_y;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 // Splits of one (row, KV head) up to this count run as one thread-block
 // cluster and merge through distributed shared memory (no workspace); more
@@ -32,6 +65,22 @@ struct DecodeArgs {
   int32_t blocks_per_split;
   int32_t num_splits;
   float scale_log2;           // scale * log2(e)
+  // Workspace slots per row and the first slot this launch writes (split s
+  // goes to slot part_slot0 + s); both default to (num_splits, 0).
+  int32_t part_slots;
+  int32_t part_slot0;
+  // Decode: per-request first block (suffix after a shared prefix handled
+  // elsewhere); NULL = 0.  Rows whose start is 0 also mark slots
+  // [0, part_slot0) empty (-inf) so the combine ignores them.
+  const int32_t* seq_start_block;
+  // Tensor-core kernel, cascade mode: group g's members are
+  // group_seqs[16g .. 16g+15] (-1 = none) and share blocks [0, group_blocks[g]).
+  const int32_t* group_seqs;
+  const int32_t* group_blocks;
+  // Decode launched right after the cascade's prefix pass: its inputs were
+  // complete before that pass started, so it starts at once (overlapping the
+  // pass) and waits for the pass only before it exits.
+  int32_t overlap_previous;
 };
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
@@ -41,15 +90,23 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, int32_t num_blocks, i
 // num_splits == 1: direct; part_o == NULL: cluster merge (num_splits <= kMaxClusterSplits);
 // otherwise partials to the workspace (the caller then runs the combine kernel).
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
+// Always writes split partials to the workspace (any number of splits).
+cudaError_t launch_paged_decode_workspace(const DecodeArgs& a, cudaStream_t stream);
 
 // Queries per request at or above which the tensor-core chunk kernel runs
 // (16 positions x 4 heads = 64 rows, one tcgen05 M=64 tile).
 constexpr int kTcMinQLen = 16;
 
 // Chunked causal attention on tensor cores (paged_chunk_tc.cu).  Same fields
-// as DecodeArgs; num_splits > 1 always goes through the workspace.
+// as DecodeArgs; num_splits > 1 always goes through the workspace.  With
+// group_seqs set (cascade mode) the grid's x index is a prefix group, the 64
+// rows are its 16 members x 4 heads (q_len 1) and the keys are the group's
+// shared prefix blocks, read through the first member's table row.
 using ChunkArgs = DecodeArgs;
-cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
+cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, int32_t grid_x, cudaStream_t stream);
+
+// Members per cascade group: 16 requests x 4 heads = one 64-row tile.
+constexpr int kCascadeGroup = 16;
 
 cudaError_t launch_attn_combine(void* out, float* out_lse, const float* part_o, const float* part_lse,
                                 int32_t num_rows, int32_t num_splits, cudaStream_t stream);

@@ -205,6 +205,35 @@ def build(
     )
 
 
+def prefix_groups(w: Workload, max_members: int = 16):
+    """Cascade description of a workload's shared prefix, as the caller that
+    built the block tables would state it: requests whose tables start with
+    the same `shared_prefix_blocks` physical blocks, in groups of at most
+    `max_members`.  Returns (group_seqs int32 [G][16] with -1 padding,
+    group_blocks int32 [G], seq_prefix_blocks int32 [B])."""
+    p = w.shared_prefix_blocks
+    seq_pre = np.zeros(w.num_seqs, np.int32)
+    if p == 0:
+        return np.zeros((0, 16), np.int32), np.zeros(0, np.int32), seq_pre
+    head = w.block_tables[:, :p]
+    sharers = [r for r in range(w.num_seqs) if -(-int(w.context_lens[r]) // BLOCK_SIZE) >= p]
+    # requests share the prefix when their first p table entries are identical
+    by_prefix = {}
+    for r in sharers:
+        by_prefix.setdefault(head[r].tobytes(), []).append(r)
+    groups = []
+    for members in by_prefix.values():
+        if len(members) < 2:
+            continue
+        for i in range(0, len(members), max_members):
+            groups.append(members[i:i + max_members])
+    gs = np.full((len(groups), 16), -1, np.int32)
+    for gi, members in enumerate(groups):
+        gs[gi, :len(members)] = members
+        seq_pre[members] = p
+    return gs, np.full(len(groups), p, np.int32), seq_pre
+
+
 # ---------------------------------------------------------------------------
 # The five workloads.  Each returns one layer's inputs; multi-layer runs draw
 # one Workload per layer (or fill per-layer pools on the device) with the same
