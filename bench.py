@@ -220,6 +220,7 @@ def main():
     ap.add_argument("--kv-blocks-per-split", type=int, default=0)
     ap.add_argument("--graph", action="store_true", help="replay each step as one CUDA graph")
     ap.add_argument("--prefix-blocks-per-split", type=int, default=0, help="cascade prefix pass split (0 = plan)")
+    ap.add_argument("--suffix-blocks-per-split", type=int, default=0, help="cascade suffix pass split (0 = plan)")
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workloads: plain paged attention instead of the cascade call")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -289,12 +290,14 @@ def main():
     cascade = (not args.no_cascade) and gs_h.shape[0] > 0 and ql == 1
     if cascade:
         maxp = int(gb_h.max())
-        pbps, sbps = pkv.cascade_plan(b, hkv, gs_h.shape[0], maxp, maxb)
+        maxs = W.max_suffix_blocks(w, sp_h)
+        pbps, sbps = pkv.cascade_plan(b, hkv, gs_h.shape[0], maxp, maxs)
         pbps = args.prefix_blocks_per_split or pbps
-        cws = torch.empty(max(256, pkv.cascade_workspace_size(b, hq, maxp, maxb, pbps, sbps)), dtype=torch.uint8,
+        sbps = args.suffix_blocks_per_split or sbps
+        cws = torch.empty(max(256, pkv.cascade_workspace_size(b, hq, maxp, maxs, pbps, sbps)), dtype=torch.uint8,
                           device=dev)
         gs_d, gb_d, sp_d = (torch.from_numpy(x).to(dev) for x in (gs_h, gb_h, sp_h))
-        splits = -(-maxp // pbps) + -(-maxb // sbps)
+        splits = -(-maxp // pbps) + -(-maxs // sbps)
         launches_per_layer = 1 + 3
 
     def check(st, what):
@@ -311,7 +314,7 @@ def main():
             check(lib.pkv_paged_attention_cascade(
                 out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride, kp0 + l * pool_stride,
                 vp0 + l * pool_stride, ctypes.byref(desc), tables.data_ptr(), maxb, ctx.data_ptr(), b, hq, w.scale,
-                gs_d.data_ptr(), gb_d.data_ptr(), sp_d.data_ptr(), gs_h.shape[0], maxp, pbps, sbps, cws.data_ptr(),
+                gs_d.data_ptr(), gb_d.data_ptr(), sp_d.data_ptr(), gs_h.shape[0], maxp, maxs, pbps, sbps, cws.data_ptr(),
                 cws.numel(), sp), "paged_attention_cascade")
         else:
             check(lib.pkv_paged_attention(out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride,
@@ -384,7 +387,7 @@ def main():
                 pkv.kv_append(k_pool[l], v_pool[l], slots, kn[l], vn[l])
                 if cascade:
                     pkv.paged_attention_cascade(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, w.scale, gs_d, gb_d,
-                                                sp_d, maxp, cws, pbps, sbps)
+                                                sp_d, maxp, maxs, cws, pbps, sbps)
                 else:
                     pkv.paged_attention(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, ql, w.scale,
                                         kv_blocks_per_split=bps, workspace=ws)
@@ -437,7 +440,8 @@ def main():
                    "layers": layers, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16,
                    "ctx_min": int(w.context_lens.min()), "ctx_max": int(w.context_lens.max()),
                    "kv_blocks_per_split": bps, "splits": splits, "cuda_graph": bool(graph is not None),
-                   "cascade": ({"groups": int(gs_h.shape[0]), "prefix_blocks": maxp, "prefix_blocks_per_split": pbps,
+                   "cascade": ({"groups": int(gs_h.shape[0]), "prefix_blocks": maxp, "max_suffix_blocks": maxs,
+                                "prefix_blocks_per_split": pbps,
                                 "suffix_blocks_per_split": sbps} if cascade else None),
                    "l2": "inputs larger than L2: one KV pool per layer, %.1f GB total" % (
                        2 * k_pool.numel() * 2 / 1e9),

@@ -176,6 +176,10 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
  *                       belongs to at most one group.
  *   num_groups        : >= 0 (0: every request is a plain decode).
  *   max_prefix_blocks : host upper bound of every P_g (sizes the prefix split).
+ *   max_suffix_blocks : host upper bound, over all requests, of the blocks
+ *                       left after the request's prefix (ceil(ctx/16) - P_g,
+ *                       or ceil(ctx/16) outside every group); 0 means
+ *                       max_blocks_per_seq.  Sizes the suffix split grid.
  *   prefix_blocks_per_split, suffix_blocks_per_split : 0 = pkv_cascade_plan.
  *   workspace         : >= pkv_cascade_workspace_size(...) bytes, 256-aligned.
  * Every other argument is as for pkv_paged_attention with q_len = 1.  A member
@@ -183,11 +187,11 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
  * prefix rows are masked at its own context), it only saves nothing.
  */
 void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups, int32_t max_prefix_blocks,
-                      int32_t max_blocks_per_seq, int32_t sm_count, int32_t* prefix_blocks_per_split,
+                      int32_t max_suffix_blocks, int32_t sm_count, int32_t* prefix_blocks_per_split,
                       int32_t* suffix_blocks_per_split);
 
 size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_prefix_blocks,
-                                  int32_t max_blocks_per_seq, int32_t prefix_blocks_per_split,
+                                  int32_t max_suffix_blocks, int32_t prefix_blocks_per_split,
                                   int32_t suffix_blocks_per_split);
 
 pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -196,9 +200,9 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
                                        int32_t num_seqs, int32_t num_q_heads, float scale,
                                        const int32_t* group_seqs, const int32_t* group_blocks,
                                        const int32_t* seq_prefix_blocks, int32_t num_groups,
-                                       int32_t max_prefix_blocks, int32_t prefix_blocks_per_split,
-                                       int32_t suffix_blocks_per_split, void* workspace,
-                                       size_t workspace_bytes, void* stream);
+                                       int32_t max_prefix_blocks, int32_t max_suffix_blocks,
+                                       int32_t prefix_blocks_per_split, int32_t suffix_blocks_per_split,
+                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of the scratch array compiled into libpkv for
  * pkv_paged_attention_static_workspace (held on every GPU that loads the

@@ -67,7 +67,7 @@ def _load():
     lib.pkv_cascade_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.pkv_cascade_workspace_size.restype = sz
     lib.pkv_paged_attention_cascade.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32, f32,
-                                                p, p, p, i32, i32, i32, i32, p, sz, p]
+                                                p, p, p, i32, i32, i32, i32, i32, p, sz, p]
     lib.pkv_paged_attention_cascade.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.pkv_get_device_error.restype = ctypes.c_int
@@ -183,25 +183,26 @@ def paged_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v
 
 
 def cascade_plan(num_seqs: int, num_kv_heads: int, num_groups: int, max_prefix_blocks: int,
-                 max_blocks_per_seq: int, sm_count: int = 0):
+                 max_suffix_blocks: int, sm_count: int = 0):
     """(prefix_blocks_per_split, suffix_blocks_per_split) the cascade call would choose."""
     pb, sb = ctypes.c_int32(0), ctypes.c_int32(0)
-    _lib.pkv_cascade_plan(num_seqs, num_kv_heads, num_groups, max_prefix_blocks, max_blocks_per_seq, sm_count,
+    _lib.pkv_cascade_plan(num_seqs, num_kv_heads, num_groups, max_prefix_blocks, max_suffix_blocks, sm_count,
                           ctypes.byref(pb), ctypes.byref(sb))
     return int(pb.value), int(sb.value)
 
 
-def cascade_workspace_size(num_seqs: int, num_q_heads: int, max_prefix_blocks: int, max_blocks_per_seq: int,
+def cascade_workspace_size(num_seqs: int, num_q_heads: int, max_prefix_blocks: int, max_suffix_blocks: int,
                            prefix_blocks_per_split: int, suffix_blocks_per_split: int) -> int:
-    return int(_lib.pkv_cascade_workspace_size(num_seqs, num_q_heads, max_prefix_blocks, max_blocks_per_seq,
+    return int(_lib.pkv_cascade_workspace_size(num_seqs, num_q_heads, max_prefix_blocks, max_suffix_blocks,
                                                prefix_blocks_per_split, suffix_blocks_per_split))
 
 
 def paged_attention_cascade(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                             block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                             group_seqs: torch.Tensor, group_blocks: torch.Tensor, seq_prefix_blocks: torch.Tensor,
-                            max_prefix_blocks: int, workspace: torch.Tensor, prefix_blocks_per_split: int = 0,
-                            suffix_blocks_per_split: int = 0, stream=None) -> None:
+                            max_prefix_blocks: int, max_suffix_blocks: int, workspace: torch.Tensor,
+                            prefix_blocks_per_split: int = 0, suffix_blocks_per_split: int = 0,
+                            stream=None) -> None:
     """Decode attention (q_len 1) with shared prefixes contracted once per group of <= 16 sharers.
 
     group_seqs int32 [G][16] (-1 = unused), group_blocks int32 [G], seq_prefix_blocks int32 [B];
@@ -224,8 +225,8 @@ def paged_attention_cascade(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
         out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
         block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), b, q.shape[2], float(scale),
         group_seqs.data_ptr() if g else 0, group_blocks.data_ptr() if g else 0, seq_prefix_blocks.data_ptr(), g,
-        int(max_prefix_blocks), int(prefix_blocks_per_split), int(suffix_blocks_per_split), ws_ptr, ws_bytes,
-        _stream_ptr(stream)), "pkv_paged_attention_cascade")
+        int(max_prefix_blocks), int(max_suffix_blocks), int(prefix_blocks_per_split), int(suffix_blocks_per_split),
+        ws_ptr, ws_bytes, _stream_ptr(stream)), "pkv_paged_attention_cascade")
 
 
 def attn_combine(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.Tensor,

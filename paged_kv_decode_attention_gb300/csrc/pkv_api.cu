@@ -198,7 +198,7 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
 }
 
 void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups, int32_t max_prefix_blocks,
-                      int32_t max_blocks_per_seq, int32_t sm_count, int32_t* prefix_blocks_per_split,
+                      int32_t max_suffix_blocks, int32_t sm_count, int32_t* prefix_blocks_per_split,
                       int32_t* suffix_blocks_per_split) {
   if (sm_count <= 0) sm_count = device_sm_count();
   const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
@@ -211,10 +211,9 @@ void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups
     pbps = ((pbps + 3) / 4) * 4;  // whole 4-block tiles
     if (pbps < 16) pbps = 16;
   }
-  // suffix pass: the decode heuristic over the part of the longest table past
-  // the longest prefix
-  int32_t span = max_blocks_per_seq - (max_prefix_blocks > 0 ? max_prefix_blocks : 0);
-  int32_t sbps = pkv_choose_kv_blocks_per_split(num_seqs, num_kv_heads, 1, span > 0 ? span : 1, sm_count);
+  // suffix pass: the decode heuristic over the longest suffix
+  const int32_t span = max_suffix_blocks > 0 ? max_suffix_blocks : 1;
+  int32_t sbps = pkv_choose_kv_blocks_per_split(num_seqs, num_kv_heads, 1, span, sm_count);
   if (prefix_blocks_per_split) *prefix_blocks_per_split = pbps;
   if (suffix_blocks_per_split) *suffix_blocks_per_split = sbps;
 }
@@ -222,13 +221,13 @@ void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups
 static int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
 size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_prefix_blocks,
-                                  int32_t max_blocks_per_seq, int32_t prefix_blocks_per_split,
+                                  int32_t max_suffix_blocks, int32_t prefix_blocks_per_split,
                                   int32_t suffix_blocks_per_split) {
-  if (num_seqs <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || prefix_blocks_per_split <= 0 ||
+  if (num_seqs <= 0 || num_q_heads <= 0 || max_suffix_blocks <= 0 || prefix_blocks_per_split <= 0 ||
       suffix_blocks_per_split <= 0)
     return 0;
   const size_t slots = static_cast<size_t>(max_prefix_blocks > 0 ? ceil_div(max_prefix_blocks, prefix_blocks_per_split) : 0) +
-                       ceil_div(max_blocks_per_seq, suffix_blocks_per_split);
+                       ceil_div(max_suffix_blocks, suffix_blocks_per_split);
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
   return align_up(rows * slots * kHeadDim * sizeof(float), 256) + align_up(rows * slots * sizeof(float), 256);
 }
@@ -238,14 +237,16 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
                                        int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
                                        int32_t num_q_heads, float scale, const int32_t* group_seqs,
                                        const int32_t* group_blocks, const int32_t* seq_prefix_blocks,
-                                       int32_t num_groups, int32_t max_prefix_blocks,
+                                       int32_t num_groups, int32_t max_prefix_blocks, int32_t max_suffix_blocks,
                                        int32_t prefix_blocks_per_split, int32_t suffix_blocks_per_split,
                                        void* workspace, size_t workspace_bytes, void* stream) {
   pkv_status st = check_cache(cache);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_blocks_per_seq < 1 || num_groups < 0 || max_prefix_blocks < 0 ||
-      max_prefix_blocks > max_blocks_per_seq || prefix_blocks_per_split < 0 || suffix_blocks_per_split < 0)
+      max_prefix_blocks > max_blocks_per_seq || max_suffix_blocks < 0 || max_suffix_blocks > max_blocks_per_seq ||
+      prefix_blocks_per_split < 0 || suffix_blocks_per_split < 0)
     return PKV_ERR_SHAPE;
+  if (max_suffix_blocks == 0) max_suffix_blocks = max_blocks_per_seq;
   if (num_q_heads != kGroup * cache->num_kv_heads) return PKV_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return PKV_ERR_SHAPE;
   if (num_seqs == 0) return PKV_OK;
@@ -257,14 +258,14 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
   int32_t pbps = prefix_blocks_per_split, sbps = suffix_blocks_per_split;
   if (pbps == 0 || sbps == 0) {
     int32_t p0 = 0, s0 = 0;
-    pkv_cascade_plan(num_seqs, cache->num_kv_heads, num_groups, max_prefix_blocks, max_blocks_per_seq, 0, &p0, &s0);
+    pkv_cascade_plan(num_seqs, cache->num_kv_heads, num_groups, max_prefix_blocks, max_suffix_blocks, 0, &p0, &s0);
     if (pbps == 0) pbps = p0;
     if (sbps == 0) sbps = s0;
   }
   const int32_t sp = (num_groups > 0 && max_prefix_blocks > 0) ? ceil_div(max_prefix_blocks, pbps) : 0;
-  const int32_t ss = ceil_div(max_blocks_per_seq, sbps);
+  const int32_t ss = ceil_div(max_suffix_blocks, sbps);
   if (sp > 65535 || ss > 65535) return PKV_ERR_UNSUPPORTED;
-  const size_t need = pkv_cascade_workspace_size(num_seqs, num_q_heads, max_prefix_blocks, max_blocks_per_seq, pbps, sbps);
+  const size_t need = pkv_cascade_workspace_size(num_seqs, num_q_heads, max_prefix_blocks, max_suffix_blocks, pbps, sbps);
   if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;

@@ -26,15 +26,16 @@ def run_cascade(w, gs, gb, sp, pbps=0, sbps=0, append=True, d=None):
     if append:
         pkv.kv_append(d["k_cache"], d["v_cache"], d["slot_mapping"], d["k_new"], d["v_new"])
     maxp = int(gb.max()) if gb.size else 0
-    p0, s0 = pkv.cascade_plan(w.num_seqs, w.num_kv_heads, gs.shape[0], maxp, w.max_blocks_per_seq)
+    maxs = W.max_suffix_blocks(w, sp)
+    p0, s0 = pkv.cascade_plan(w.num_seqs, w.num_kv_heads, gs.shape[0], maxp, maxs)
     pbps, sbps = pbps or p0, sbps or s0
-    ws = torch.empty(max(1, pkv.cascade_workspace_size(w.num_seqs, w.num_q_heads, maxp, w.max_blocks_per_seq,
-                                                       pbps, sbps)), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(1, pkv.cascade_workspace_size(w.num_seqs, w.num_q_heads, maxp, maxs, pbps, sbps)),
+                     dtype=torch.uint8, device="cuda")
     out = torch.full_like(d["q"], float("nan"))
     gs_d = dev(gs) if gs.size else torch.zeros((0, 16), dtype=torch.int32, device="cuda")
     gb_d = dev(gb) if gb.size else torch.zeros(0, dtype=torch.int32, device="cuda")
     pkv.paged_attention_cascade(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
-                                w.scale, gs_d, gb_d, dev(sp), maxp, ws, pbps, sbps)
+                                w.scale, gs_d, gb_d, dev(sp), maxp, maxs, ws, pbps, sbps)
     torch.cuda.synchronize()
     assert pkv.get_device_error(reset=True) == 0
     return out

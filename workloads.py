@@ -234,6 +234,12 @@ def prefix_groups(w: Workload, max_members: int = 16):
     return gs, np.full(len(groups), p, np.int32), seq_pre
 
 
+def max_suffix_blocks(w: Workload, seq_prefix_blocks: np.ndarray) -> int:
+    """Longest run of blocks any request has after its shared prefix."""
+    need = np.array([-(-int(c) // BLOCK_SIZE) for c in w.context_lens])
+    return int(max(1, (need - seq_prefix_blocks).max()))
+
+
 # ---------------------------------------------------------------------------
 # The five workloads.  Each returns one layer's inputs; multi-layer runs draw
 # one Workload per layer (or fill per-layer pools on the device) with the same
