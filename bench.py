@@ -154,11 +154,17 @@ def barrier(world):
         dist.barrier()
 
 
+def aggregate_gbs(world: int, step_bytes: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes one replica of the step; time is the max over ranks."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 def all_max(x: float, world: int) -> float:
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    on_gpu = torch.cuda.is_available() and dist.get_backend() == "nccl"
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -425,7 +431,7 @@ def main():
     if not peak:
         peak, peak_src = 6800.0, "fallback"
     achieved = attn_b / (attn_us * 1e-6) / 1e9
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = aggregate_gbs(world, step_bytes, ms_per_step)
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
