@@ -119,17 +119,20 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
   const int n_tiles = (b1 - b0 + kTileBlocks - 1) / kTileBlocks;
 
   // rows handled by softmax threads: warp w >= 2 owns TMEM sub-partition w % 4
+  // Threads t and t+16 of a softmax warp share one row (TMEM lane t), each
+  // taking half of its columns.
   const int quad = warp & 3;
-  const int row = quad * 16 + lane;  // meaningful for lane < 16
-  const int rq = (warp >= 2 && lane < 16) ? row_req(row) : -1;
+  const int half = lane >> 4;
+  const int row = quad * 16 + (lane & 15);
+  const int rq = warp >= 2 ? row_req(row) : -1;
   const int ip = row_pos(row);
   const int g = row & 3;
-  const bool row_valid = warp >= 2 && lane < 16 && rq >= 0 && ip < a.q_len;
+  const bool row_valid = warp >= 2 && rq >= 0 && ip < a.q_len;
   const int64_t orow = (static_cast<int64_t>(rq) * a.q_len + ip) * hq + kvh * kGroup + g;
   const int64_t slot = orow * a.part_slots + a.part_slot0 + split;
 
   if (n_tiles <= 0) {
-    if (row_valid) {
+    if (row_valid && half == 0) {
       if constexpr (kSplit) {
         a.part_lse[slot] = -INFINITY;
       } else {
@@ -285,8 +288,9 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       const int ctx_r = a.context_lens[rq];
       n_vis_row = min(min(max(ctx_r - a.q_len + 1 + ip, 0), cap), b1 * kBlockSize);
     }
-    float m_stale = -INFINITY;  // max the weights are taken against (lags the true max by < 2^8)
-    float l = 0.f;
+    const float c = a.scale_log2;  // > 0: the max of raw scores scales to the max of scaled ones
+    float m_stale = -INFINITY;     // scaled max the weights are taken against (lags the true max by < 2^8)
+    float l = 0.f;                 // this thread's half of the row's weight sum
     for (int j = 0; j < n_tiles && ok; ++j) {
       const int sb = j & 1;
       const int st = j % kTcStages;
@@ -294,23 +298,21 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j >> 1) & 1));
       if (!ok) break;
       tc::fence_after_sync();
-      float s[kTileTokens];
-      tc::tmem_ld32(tmem + lane_off + sb * 64, s);
-      tc::tmem_ld32(tmem + lane_off + sb * 64 + 32, s + 32);
+      float s[32];  // raw scores of tokens half*32 .. half*32+31 of the tile
+      tc::tmem_ld16x2_32<32>(tmem + lane_off + sb * 64, s);
       tc::tmem_wait_ld();
-      const int tok0 = (b0 + j * kTileBlocks) * kBlockSize;
+      const int tok0 = (b0 + j * kTileBlocks) * kBlockSize + half * 32;
+      if (__any_sync(0xffffffffu, tok0 + 32 > n_vis_row)) {
 #pragma unroll
-      for (int c = 0; c < kTileTokens; ++c) s[c] = (tok0 + c < n_vis_row) ? s[c] * a.scale_log2 : -INFINITY;
+        for (int e = 0; e < 32; ++e) s[e] = (tok0 + e < n_vis_row) ? s[e] : -INFINITY;
+      }
       float mx;
       {
         float t8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float u = fmaxf(fmaxf(s[e], s[e + 8]), fmaxf(s[e + 16], s[e + 24]));
-          float v = fmaxf(fmaxf(s[e + 32], s[e + 40]), fmaxf(s[e + 48], s[e + 56]));
-          t8[e] = fmaxf(u, v);
-        }
+        for (int e = 0; e < 8; ++e) t8[e] = fmaxf(fmaxf(s[e], s[e + 8]), fmaxf(s[e + 16], s[e + 24]));
         mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * c;  // whole row, scaled
       }
       const bool grow = mx > m_stale + kRescaleThreshold;  // also true the first time a row sees a key
       const float m_new = grow ? mx : m_stale;
@@ -320,36 +322,39 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1));
         tc::fence_after_sync();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           float o[32];
-          tc::tmem_ld32(tmem + lane_off + kColO + 32 * cc, o);
+          tc::tmem_ld16x2_32<64>(tmem + lane_off + kColO + 32 * cc, o);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tc::tmem_st32(tmem + lane_off + kColO + 32 * cc, o);
+          tc::tmem_st16x2_32<64>(tmem + lane_off + kColO + 32 * cc, o);
         }
         tc::tmem_wait_st();
       }
       l *= alpha;
       m_stale = m_new;
-      const float m_use = (m_stale == -INFINITY) ? 0.f : m_stale;
+      const float nm = (m_stale == -INFINITY) ? 0.f : -m_stale;
+      const float2 c2 = make_float2(c, c);
+      const float2 nm2 = make_float2(nm, nm);
       // P_j overwrites the S_j buffer it came from: 2 BF16 per 32-bit column
-      float pk[32];
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[16];
+      float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = exp2_approx(s[2 * c] - m_use);
-        const float p1 = exp2_approx(s[2 * c + 1] - m_use);
-        rs8[c & 7] += p0 + p1;
-        pk[c] = __uint_as_float(pack_bf16x2(p0, p1));
+      for (int e = 0; e < 16; ++e) {
+        const float2 x = __ffma2_rn(make_float2(s[2 * e], s[2 * e + 1]), c2, nm2);
+        const float p0 = exp2_approx(x.x);
+        const float p1 = exp2_approx(x.y);
+        acc2 = __fadd2_rn(acc2, make_float2(p0, p1));
+        pk[e] = pack_bf16x2(p0, p1);
       }
-      tc::tmem_st32(tmem + lane_off + sb * 64, pk);
-      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-      l += rs;
+      tc::tmem_st16x2_16<16>(tmem + lane_off + sb * 64, pk);
+      l += acc2.x + acc2.y;
       // slots past the request's data in its last block may hold anything: zero those V rows
-      const int tile_end = tok0 + kTileTokens;
-      if (ctx_keys < tile_end && ctx_keys > tok0 && (ctx_keys & (kBlockSize - 1)) != 0) {
-        const int first = ctx_keys - tok0;                                // first garbage token of the tile
+      const int tile0 = (b0 + j * kTileBlocks) * kBlockSize;
+      const int tile_end = tile0 + kTileTokens;
+      if (ctx_keys < tile_end && ctx_keys > tile0 && (ctx_keys & (kBlockSize - 1)) != 0) {
+        const int first = ctx_keys - tile0;                                // first garbage token of the tile
         const int last = min(kTileTokens, ((first + kBlockSize - 1) / kBlockSize) * kBlockSize);
         uint8_t* vt = smem + kOffKV + st * kStageBytesTc + 2 * kHalfBytes;
         const int t128 = threadIdx.x - 64;
@@ -365,24 +370,26 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       mbar_arrive(&bars->p_full[sb]);
     }
     if (!ok && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
-    // ---- epilogue ----
+    // ---- epilogue: this thread writes dims half*64 .. half*64+63 of its row ----
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1));
     tc::fence_after_sync();
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
-    const float lse = (l > 0.f) ? (m_stale + log2f(l)) * kLn2 : -INFINITY;
+    const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
+    const float inv = (l_row > 0.f) ? 1.f / l_row : 0.f;
+    const float lse = (l_row > 0.f) ? (m_stale + log2f(l_row)) * kLn2 : -INFINITY;
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < 2; ++cc) {
       float o[32];
-      tc::tmem_ld32(tmem + lane_off + kColO + 32 * cc, o);
+      tc::tmem_ld16x2_32<64>(tmem + lane_off + kColO + 32 * cc, o);  // dims half*64 + 32cc .. +31
       tc::tmem_wait_ld();
+      const int d0 = half * 64 + 32 * cc;
       if (row_valid && ok) {
         if constexpr (kSplit) {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kHeadDim + 32 * cc);
+          float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kHeadDim + d0);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim + 32 * cc);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim + d0);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 w;
@@ -396,7 +403,7 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       }
     }
     if constexpr (kSplit) {
-      if (row_valid && ok) a.part_lse[slot] = lse;
+      if (row_valid && ok && half == 0) a.part_lse[slot] = lse;
     }
   }
 
