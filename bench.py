@@ -236,9 +236,15 @@ def main():
     ap.add_argument("--oracle-budget-s", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--num-seqs", type=int, default=0, help="chunk workload: fewer requests (small profiling cases)")
+    ap.add_argument("--sweep", action="store_true", help="q_len-1 batch x context sweep instead of a step benchmark")
+    ap.add_argument("--sweep-batches", default="", help="comma list (default 1..512, powers of two)")
+    ap.add_argument("--sweep-contexts", default="", help="comma list (default 128..65536, powers of two)")
+    ap.add_argument("--sweep-reps", type=int, default=10)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    if args.sweep:
+        return run_sweep(args)
     world, rank, local = dist_init(args.gpus)
     w, layers = make_workload(args.workload, args.seed, args.num_seqs)
     if args.layers > 0:
@@ -478,6 +484,63 @@ def main():
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_sweep(args):
+    """q_len-1 stress sweep: batch x context grid, one layer, default split;
+    L2 flushed (a 256 MiB write) before every timed call so small points are
+    read from HBM too.  Prints one JSON line with every point."""
+    import paged_kv_decode_attention_gb300 as pkv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    free, _ = torch.cuda.mem_get_info(dev)
+    batches = [int(x) for x in args.sweep_batches.split(",")] if args.sweep_batches else W.SWEEP_BATCHES
+    contexts = [int(x) for x in args.sweep_contexts.split(",")] if args.sweep_contexts else W.SWEEP_CONTEXTS
+    peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("hbm_gbs", 6800.0) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else 6800.0
+    points = []
+    for b in batches:
+        for c in contexts:
+            nb = b * (-(-c // 16)) + 8
+            pool_bytes = 2 * nb * 8 * 16 * 128 * 2
+            if pool_bytes > 0.8 * free:
+                points.append({"batch": b, "ctx": c, "skipped": "pool larger than free device memory"})
+                continue
+            w = W.build(f"sweep", [c] * b, nb, seed=b * 7919 + c, fill_cache=False)
+            kc = torch.empty((nb, 8, 16, 128), dtype=torch.bfloat16, device=dev)
+            vc = torch.empty_like(kc)
+            W.fill_pool_device(kc, 2 * b + 1)
+            W.fill_pool_device(vc, 2 * b + 2)
+            q = torch.from_numpy(w.q).view(torch.bfloat16).to(dev)
+            tables = torch.from_numpy(w.block_tables).to(dev)
+            ctx = torch.from_numpy(w.context_lens).to(dev)
+            out = torch.empty_like(q)
+            maxb = w.max_blocks_per_seq
+            bps = pkv.choose_kv_blocks_per_split(b, 8, 1, maxb)
+            ws = torch.empty(max(256, pkv.workspace_size(b, 1, 32, maxb, bps)), dtype=torch.uint8, device=dev)
+            times = []
+            for it in range(args.warmup + args.sweep_reps):
+                flush.fill_(it & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                pkv.paged_attention(out, q, kc, vc, tables, ctx, 1, w.scale, kv_blocks_per_split=bps, workspace=ws)
+                e1.record(stream)
+                e1.synchronize()
+                if it >= args.warmup:
+                    times.append(e0.elapsed_time(e1))
+            us = statistics.median(times) * 1e3
+            attn_b, _ = bytes_per_layer(w)
+            points.append({"batch": b, "ctx": c, "us": round(us, 2), "gbs": round(attn_b / (us * 1e-6) / 1e9, 1),
+                           "frac": round(attn_b / (us * 1e-6) / 1e9 / peak, 4), "splits": -(-maxb // bps)})
+            del kc, vc, q, out, ws
+            torch.cuda.empty_cache()
+    if pkv.get_device_error(reset=True) != 0:
+        raise RuntimeError("device error word set during the sweep")
+    print(json.dumps({"metric": "paged decode attention sweep (q_len 1, one layer, L2 flushed)", "peak_gbs": peak,
+                      "reps": args.sweep_reps, "points": points}), flush=True)
 
 
 def kernel_build_id() -> str:

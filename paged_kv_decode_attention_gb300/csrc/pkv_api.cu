@@ -113,7 +113,9 @@ int32_t pkv_choose_kv_blocks_per_split(int32_t num_seqs, int32_t num_kv_heads, i
   const int64_t rows = static_cast<int64_t>(num_seqs) * (q_len > 0 ? q_len : 1) * num_kv_heads;
   const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
   if (rows <= 0 || max_blocks_per_seq <= kMinBlocksPerSplit) return max_blocks_per_seq;
-  const int64_t splits = (slots + rows / 2) / rows;  // nearest whole number of splits to one wave
+  // as many splits as fit in one wave: a few CTAs spilling into a second wave
+  // would double the call's time
+  const int64_t splits = slots / rows;
   if (splits <= 1) return max_blocks_per_seq;
   int64_t bps = (max_blocks_per_seq + splits - 1) / splits;
   if (bps < kMinBlocksPerSplit) bps = kMinBlocksPerSplit;
