@@ -97,6 +97,36 @@ __device__ __forceinline__ void unpack8x2(const uint4 v, float2* f) {
   f[3] = bf16x2_to_float2(v.w);
 }
 
+constexpr float kLog2eF = 1.4426950408889634f;
+
+// Fold the cascade prefix pass's partials of one output row into a running
+// (max in base-2 logits, weight sum, un-normalised dims d0..d0+3).  A partial
+// (normalised O_s, natural-log lse_s) is a block of total weight 1 at the
+// base-2 logit lse_s * log2 e.
+__device__ __forceinline__ void fold_prefix(const DecodeArgs& a, int64_t orow, int d0, float& mx, float& sum,
+                                            float* o) {
+  const float* lse = a.prefix_lse + orow * a.prefix_slots;
+  float m2 = mx;
+  for (int sl = 0; sl < a.prefix_slots; ++sl) m2 = fmaxf(m2, lse[sl] * kLog2eF);
+  if (m2 == -INFINITY) return;
+  const float sc_old = exp2_approx(mx - m2);  // 0 when nothing was accumulated yet
+  sum *= sc_old;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) o[e] *= sc_old;
+  for (int sl = 0; sl < a.prefix_slots; ++sl) {
+    const float ls = lse[sl];
+    if (ls == -INFINITY) continue;
+    const float w = exp2_approx(ls * kLog2eF - m2);
+    sum += w;
+    const float4 v = *reinterpret_cast<const float4*>(a.prefix_o + (orow * a.prefix_slots + sl) * kHeadDim + d0);
+    o[0] = fmaf(w, v.x, o[0]);
+    o[1] = fmaf(w, v.y, o[1]);
+    o[2] = fmaf(w, v.z, o[2]);
+    o[3] = fmaf(w, v.w, o[3]);
+  }
+  mx = m2;
+}
+
 template <int NS, SplitMode kMode>
 __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
   using L = DecodeSmem<NS>;
@@ -134,8 +164,24 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
   const int64_t qrow0 = static_cast<int64_t>(vrow) * hq + kvh * kGroup;  // (r, i, first head of group)
   const bool empty = b0 >= b1;
 
+  const bool has_prefix = a.prefix_o != nullptr && start > 0;
   if (empty) {  // nothing to read: padding row, query without keys, or a split past the context
     if constexpr (kMode == SplitMode::kDirect) {
+      if (has_prefix) {
+        // the whole context lies in the shared prefix: the result is the prefix pass's
+        if (threadIdx.x < kGroup * 32) {
+          const int hh = threadIdx.x >> 5, dd = (threadIdx.x & 31) * 4;
+          float mx = -INFINITY, sum = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+          pdl_wait();
+          fold_prefix(a, qrow0 + hh, dd, mx, sum, o);
+          const float inv = sum > 0.f ? 1.f / sum : 0.f;
+          uint2 packed;
+          packed.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+          packed.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + (qrow0 + hh) * kHeadDim + dd) = packed;
+        }
+        return;
+      }
       if (threadIdx.x < kGroup * kRowBytes / 16)
         reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + qrow0 * kHeadDim)[threadIdx.x] =
             make_uint4(0, 0, 0, 0);
@@ -391,7 +437,13 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
           cta_l[h] = sum;
         }
       } else {
-        const float inv = (mx != -INFINITY) ? 1.f / sum : 0.f;
+        if constexpr (kMode == SplitMode::kDirect) {
+          if (has_prefix) {
+            pdl_wait();  // the prefix pass wrote these partials
+            fold_prefix(a, orow, d0, mx, sum, o);
+          }
+        }
+        const float inv = (mx != -INFINITY && sum > 0.f) ? 1.f / sum : 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[e] *= inv;
         if constexpr (kMode == SplitMode::kDirect) {
@@ -434,15 +486,20 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
           o2 = fmaf(v.z, sc, o2);
           o3 = fmaf(v.w, sc, o3);
         }
-        const float inv = 1.f / sum;
-        o0 *= inv;
-        o1 *= inv;
-        o2 *= inv;
-        o3 *= inv;
       }
+      if (has_prefix) {
+        pdl_wait();  // the prefix pass wrote these partials
+        float o4[4] = {o0, o1, o2, o3};
+        fold_prefix(a, qrow0 + h, d0, mx, sum, o4);
+        o0 = o4[0];
+        o1 = o4[1];
+        o2 = o4[2];
+        o3 = o4[3];
+      }
+      const float inv = (mx != -INFINITY && sum > 0.f) ? 1.f / sum : 0.f;
       uint2 packed;
-      packed.x = pack_bf16x2(o0, o1);
-      packed.y = pack_bf16x2(o2, o3);
+      packed.x = pack_bf16x2(o0 * inv, o1 * inv);
+      packed.y = pack_bf16x2(o2 * inv, o3 * inv);
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + (qrow0 + h) * kHeadDim + d0) = packed;
     }
     // keep every CTA's shared memory alive until CTA 0 has read it

@@ -228,8 +228,12 @@ size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t
   if (num_seqs <= 0 || num_q_heads <= 0 || max_suffix_blocks <= 0 || prefix_blocks_per_split <= 0 ||
       suffix_blocks_per_split <= 0)
     return 0;
+  // the suffix pass merges on chip (and folds in the prefix partials) when it
+  // needs at most kMaxClusterSplits splits; only then does it need no slots
+  const int32_t ss = ceil_div(max_suffix_blocks, suffix_blocks_per_split);
   const size_t slots = static_cast<size_t>(max_prefix_blocks > 0 ? ceil_div(max_prefix_blocks, prefix_blocks_per_split) : 0) +
-                       ceil_div(max_suffix_blocks, suffix_blocks_per_split);
+                       (ss > kMaxClusterSplits ? ss : 0);
+  if (slots == 0) return 0;
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
   return align_up(rows * slots * kHeadDim * sizeof(float), 256) + align_up(rows * slots * sizeof(float), 256);
 }
@@ -268,10 +272,11 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
   const int32_t ss = ceil_div(max_suffix_blocks, sbps);
   if (sp > 65535 || ss > 65535) return PKV_ERR_UNSUPPORTED;
   const size_t need = pkv_cascade_workspace_size(num_seqs, num_q_heads, max_prefix_blocks, max_suffix_blocks, pbps, sbps);
-  if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
-  const int32_t slots = sp + ss;
+  const bool on_chip = ss <= kMaxClusterSplits;  // suffix merges in a cluster and folds in the prefix
+  const int32_t slots = sp + (on_chip ? 0 : ss);
 
   DecodeArgs a{};
   a.out = out;
@@ -287,9 +292,12 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
   a.num_seqs = num_seqs;
   a.q_len = 1;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.part_o = static_cast<float*>(workspace);
-  a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                        align_up(rows * slots * kHeadDim * sizeof(float), 256));
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = slots > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                         align_up(rows * slots * kHeadDim * sizeof(float), 256))
+                              : nullptr;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
   a.part_slots = slots;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (sp > 0) {
@@ -305,9 +313,22 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
   // private suffixes (and requests outside every group) on the decode kernel
   a.blocks_per_split = sbps;
   a.num_splits = ss;
-  a.part_slot0 = sp;
   a.seq_start_block = seq_prefix_blocks;
   a.overlap_previous = sp > 0 ? 1 : 0;  // the suffix pass runs beside the prefix pass
+  if (on_chip) {
+    // direct (one split) or cluster merge, folding in the prefix partials: no combine kernel
+    a.part_o = nullptr;
+    a.part_lse = nullptr;
+    a.part_slots = 0;
+    a.part_slot0 = 0;
+    if (sp > 0) {
+      a.prefix_o = part_o;
+      a.prefix_lse = part_lse;
+      a.prefix_slots = sp;
+    }
+    return launch_paged_decode(a, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
+  a.part_slot0 = sp;
   if (launch_paged_decode_workspace(a, s) != cudaSuccess) return PKV_ERR_CUDA;
   if (launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), slots, s) != cudaSuccess)
     return PKV_ERR_CUDA;

@@ -77,6 +77,12 @@ struct DecodeArgs {
   // group_seqs[16g .. 16g+15] (-1 = none) and share blocks [0, group_blocks[g]).
   const int32_t* group_seqs;
   const int32_t* group_blocks;
+  // Decode in direct or cluster mode for a cascade: the prefix pass's
+  // normalised partials (prefix_slots per output row, natural-log lse) are
+  // merged into the final result of rows whose request has a prefix.
+  const float* prefix_o;
+  const float* prefix_lse;
+  int32_t prefix_slots;
   // Decode launched right after the cascade's prefix pass: its inputs were
   // complete before that pass started, so it starts at once (overlapping the
   // pass) and waits for the pass only before it exits.
