@@ -204,11 +204,15 @@ void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups
                       int32_t* suffix_blocks_per_split) {
   if (sm_count <= 0) sm_count = device_sm_count();
   const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
-  // prefix pass: enough (group, split, head) CTAs to fill the GPU, each at least one 64-token tile
+  // prefix pass: about a third of the SMs' worth of (group, split, head)
+  // CTAs.  The suffix pass runs beside it and needs the rest: an SM holding a
+  // tensor-core CTA has room for one decode CTA only, so many short prefix
+  // CTAs would crowd the suffix out, and few long ones would finish last.
   int32_t pbps = max_prefix_blocks > 0 ? max_prefix_blocks : 1;
   const int64_t prows = static_cast<int64_t>(num_groups > 0 ? num_groups : 1) * num_kv_heads;
-  if (max_prefix_blocks > 0 && prows < slots) {
-    const int64_t sp = (slots + prows - 1) / prows;
+  const int64_t target = (sm_count + 2) / 3;
+  if (max_prefix_blocks > 0 && prows < target) {
+    const int64_t sp = (target + prows / 2) / prows;
     pbps = static_cast<int32_t>((max_prefix_blocks + sp - 1) / sp);
     pbps = ((pbps + 3) / 4) * 4;  // whole 4-block tiles
     if (pbps < 16) pbps = 16;
