@@ -79,6 +79,11 @@ enum class SplitMode { kDirect, kCluster, kWorkspace };
 
 template <int NS>
 struct DecodeSmem {
+  // Every use of a stage must go to the same consumer warp (stage st belongs
+  // to warp st % 4): with another stage count a fast warp could wait for a
+  // stage's phase k+2 while phase k+1 is still in flight, and a parity wait
+  // cannot tell those phases apart.
+  static_assert(NS % kConsumerWarps == 0, "stage count must be a multiple of the consumer warps");
   static constexpr int kBarOffset = NS * kStageBytes;
   static constexpr int kPOffset = kBarOffset + 2 * NS * 8;                 // float [4 warps][16 tok][4 heads]
   static constexpr int kMOffset = kPOffset + kConsumerWarps * 64 * 4;      // float [4 warps][4 heads]
