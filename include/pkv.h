@@ -56,7 +56,8 @@ typedef enum pkv_status {
   PKV_ERR_SHAPE = 2,       /* a size is negative or inconsistent               */
   PKV_ERR_UNSUPPORTED = 3, /* a shape this build has no kernel for             */
   PKV_ERR_WORKSPACE = 4,   /* split-KV workspace missing or too small          */
-  PKV_ERR_CUDA = 5         /* a CUDA runtime call failed (launch, attribute)   */
+  PKV_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute)   */
+  PKV_ERR_EXHAUSTED = 6    /* a block pool has too few free blocks             */
 } pkv_status;
 
 /* Bits of the device error word (pkv_get_device_error). */
@@ -266,6 +267,61 @@ pkv_status pkv_attn_combine(void* out, float* out_lse, const float* partial_o,
  * *host_word; when reset != 0, clear it.  Synchronises the device.
  */
 pkv_status pkv_get_device_error(uint32_t* host_word, int32_t reset);
+
+/*
+ * Block pool and copy-on-write -- the host-side bookkeeping of §8.3.1/§8.3.2
+ * ("Chapter 8: Inference Optimization"): blocks come from a free pool; each
+ * block-table entry pointing at a block is a reference (Fig. 8-14: a block
+ * returns to the pool when its last reference is released); before a request
+ * writes into a shared, partly filled tail block it takes a private copy
+ * (Fig. 8-15), while full shared blocks stay shared.
+ *
+ * The pool is host memory only and is not thread-safe.  It tracks counts; it
+ * does not know when device work using a block has finished, so release a
+ * block only after the work that reads it has completed (§8.3.2: a block is
+ * reused only when no reference holds it and the accelerator no longer reads
+ * it).  block_size is the pool's tokens per block (the kernels use 16).
+ */
+typedef struct pkv_block_pool pkv_block_pool;
+
+pkv_status pkv_block_pool_create(int32_t num_blocks, int32_t block_size, pkv_block_pool** pool);
+void pkv_block_pool_destroy(pkv_block_pool* pool);
+/* Free blocks, or -1 for a NULL pool. */
+int32_t pkv_block_pool_num_free(const pkv_block_pool* pool);
+/* References held on `block`, or -1 if it is not a block of the pool. */
+int32_t pkv_block_pool_refcount(const pkv_block_pool* pool, int32_t block);
+/* n fresh blocks (one reference each) into blocks[0..n); all or nothing
+ * (PKV_ERR_EXHAUSTED, nothing taken). */
+pkv_status pkv_block_pool_alloc(pkv_block_pool* pool, int32_t n, int32_t* blocks);
+/* One more reference on each listed block (a second table now points at it). */
+pkv_status pkv_block_pool_share(pkv_block_pool* pool, const int32_t* blocks, int32_t n);
+/* Drop one reference per listed block; blocks reaching 0 return to the pool.
+ * Rejects (PKV_ERR_SHAPE, nothing changed) a release of a block without a
+ * reference to drop. */
+pkv_status pkv_block_pool_release(pkv_block_pool* pool, const int32_t* blocks, int32_t n);
+/*
+ * Make token positions ctx_before .. ctx_before+num_new-1 of one request
+ * writable: append fresh blocks to its table row (row_blocks grows, up to
+ * max_blocks) and give it a private copy of every shared block among those it
+ * already holds that the new tokens fall into.  Each copy is reported as
+ * (copy_src[i] -> copy_dst[i]), i < *num_copies (capacity: ceil(num_new /
+ * block_size) + 1 entries); the table row already points at copy_dst, so the
+ * caller runs pkv_copy_blocks on them before appending.  All or nothing.
+ */
+pkv_status pkv_block_pool_reserve(pkv_block_pool* pool, int32_t* table_row, int32_t* row_blocks,
+                                  int32_t max_blocks, int32_t ctx_before, int32_t num_new,
+                                  int32_t* copy_src, int32_t* copy_dst, int32_t* num_copies);
+
+/*
+ * pkv_copy_blocks -- copy whole physical blocks (all KV heads, K and V) from
+ * src_blocks[i] to dst_blocks[i], bit for bit: the copy half of copy-on-write.
+ * src_blocks, dst_blocks: device int32 [num_pairs]; destinations distinct and
+ * no destination also a source.  An id outside the pool skips that pair and
+ * sets PKV_DEVERR_BLOCK_ID.
+ */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                           const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                           void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* pkv_status_string(pkv_status status);

@@ -188,3 +188,11 @@ def attn_combine(partial_o: np.ndarray, partial_lse: np.ndarray):
         out[r] = (w[:, None] * po[r][finite]).sum(axis=0)
         lse[r] = total
     return out, lse
+
+
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, src_blocks, dst_blocks) -> None:
+    """In place: physical block dst <- physical block src, all heads, K and V
+    (the copy step of copy-on-write, §8.3.2 / Fig. 8-15)."""
+    for s, d in zip(src_blocks, dst_blocks):
+        k_cache[int(d)] = k_cache[int(s)]
+        v_cache[int(d)] = v_cache[int(s)]

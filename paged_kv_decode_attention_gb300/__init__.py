@@ -20,7 +20,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "PkvError", "kv_append", "paged_attention", "paged_attention_cascade", "cascade_plan",
+    "PkvError", "BlockPool", "copy_blocks", "kv_append", "paged_attention", "paged_attention_cascade", "cascade_plan",
     "cascade_workspace_size", "attn_combine", "workspace_size",
     "choose_kv_blocks_per_split", "get_device_error", "library_path", "lib", "DEVERR_BLOCK_ID",
     "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT",
@@ -69,6 +69,25 @@ def _load():
     lib.pkv_paged_attention_cascade.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32, f32,
                                                 p, p, p, i32, i32, i32, i32, i32, p, sz, p]
     lib.pkv_paged_attention_cascade.restype = ctypes.c_int
+    pp = ctypes.POINTER(i32)
+    lib.pkv_block_pool_create.argtypes = [i32, i32, ctypes.POINTER(p)]
+    lib.pkv_block_pool_create.restype = ctypes.c_int
+    lib.pkv_block_pool_destroy.argtypes = [p]
+    lib.pkv_block_pool_destroy.restype = None
+    lib.pkv_block_pool_num_free.argtypes = [p]
+    lib.pkv_block_pool_num_free.restype = i32
+    lib.pkv_block_pool_refcount.argtypes = [p, i32]
+    lib.pkv_block_pool_refcount.restype = i32
+    lib.pkv_block_pool_alloc.argtypes = [p, i32, pp]
+    lib.pkv_block_pool_alloc.restype = ctypes.c_int
+    lib.pkv_block_pool_share.argtypes = [p, pp, i32]
+    lib.pkv_block_pool_share.restype = ctypes.c_int
+    lib.pkv_block_pool_release.argtypes = [p, pp, i32]
+    lib.pkv_block_pool_release.restype = ctypes.c_int
+    lib.pkv_block_pool_reserve.argtypes = [p, pp, pp, i32, i32, i32, pp, pp, pp]
+    lib.pkv_block_pool_reserve.restype = ctypes.c_int
+    lib.pkv_copy_blocks.argtypes = [p, p, ctypes.POINTER(CacheDesc), p, p, i32, p]
+    lib.pkv_copy_blocks.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.pkv_get_device_error.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -247,6 +266,75 @@ def attn_combine(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.
         lse_ptr = out_lse.data_ptr()
     _check(_lib.pkv_attn_combine(out.data_ptr(), lse_ptr, partial_o.data_ptr(), partial_lse.data_ptr(), rows, d, s,
                                  _stream_ptr(stream)), "pkv_attn_combine")
+
+
+class BlockPool:
+    """Refcounted physical-block pool (host memory) with copy-on-write reservation.
+
+    Wraps pkv_block_pool_*: alloc / share / release blocks, and `reserve`
+    a request's table row for new tokens (fresh blocks appended, shared
+    partly-filled blocks replaced by private copies to be made with
+    copy_blocks)."""
+
+    def __init__(self, num_blocks: int, block_size: int = BLOCK_SIZE):
+        self._p = ctypes.c_void_p(0)
+        _check(_lib.pkv_block_pool_create(num_blocks, block_size, ctypes.byref(self._p)), "pkv_block_pool_create")
+        self.block_size = block_size
+
+    def close(self):
+        if self._p:
+            _lib.pkv_block_pool_destroy(self._p)
+            self._p = ctypes.c_void_p(0)
+
+    def __del__(self):
+        self.close()
+
+    @staticmethod
+    def _arr(values):
+        return (ctypes.c_int32 * max(1, len(values)))(*values)
+
+    @property
+    def num_free(self) -> int:
+        return int(_lib.pkv_block_pool_num_free(self._p))
+
+    def refcount(self, block: int) -> int:
+        return int(_lib.pkv_block_pool_refcount(self._p, block))
+
+    def alloc(self, n: int) -> list:
+        out = (ctypes.c_int32 * max(1, n))()
+        _check(_lib.pkv_block_pool_alloc(self._p, n, out), "pkv_block_pool_alloc")
+        return list(out[:n])
+
+    def share(self, blocks) -> None:
+        _check(_lib.pkv_block_pool_share(self._p, self._arr(blocks), len(blocks)), "pkv_block_pool_share")
+
+    def release(self, blocks) -> None:
+        _check(_lib.pkv_block_pool_release(self._p, self._arr(blocks), len(blocks)), "pkv_block_pool_release")
+
+    def reserve(self, table_row: list, ctx_before: int, num_new: int, max_blocks: int):
+        """Extend/privatise `table_row` (list, modified in place) for num_new tokens
+        after ctx_before; returns the list of (src, dst) block copies to make."""
+        row = (ctypes.c_int32 * max(1, max_blocks))(*table_row)
+        n = ctypes.c_int32(len(table_row))
+        cap = -(-num_new // self.block_size) + 1
+        src, dst = (ctypes.c_int32 * cap)(), (ctypes.c_int32 * cap)()
+        nc = ctypes.c_int32(0)
+        _check(_lib.pkv_block_pool_reserve(self._p, row, ctypes.byref(n), max_blocks, ctx_before, num_new, src, dst,
+                                           ctypes.byref(nc)), "pkv_block_pool_reserve")
+        table_row[:] = list(row[:n.value])
+        return [(src[i], dst[i]) for i in range(nc.value)]
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: torch.Tensor, dst_blocks: torch.Tensor,
+                stream=None) -> None:
+    """Copy physical blocks src -> dst (all heads, K and V), bit for bit."""
+    _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    _i32(src_blocks, "src_blocks"), _i32(dst_blocks, "dst_blocks")
+    if src_blocks.numel() != dst_blocks.numel():
+        raise ValueError("src_blocks and dst_blocks differ in length")
+    desc = _desc(k_cache)
+    _check(_lib.pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc), src_blocks.data_ptr(),
+                                dst_blocks.data_ptr(), src_blocks.numel(), _stream_ptr(stream)), "pkv_copy_blocks")
 
 
 def get_device_error(reset: bool = True) -> int:

@@ -23,9 +23,11 @@ constexpr int kMaxDevices = 64;
 unsigned int* g_error_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 
+}  // namespace
+
 // Address of this device's error word, looked up once per device (with that
 // device current, as cudaGetSymbolAddress requires).
-unsigned int* error_word() {
+unsigned int* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   if (g_error_ptr[dev] == nullptr) {
@@ -35,6 +37,10 @@ unsigned int* error_word() {
   }
   return g_error_ptr[dev];
 }
+
+namespace {
+
+unsigned int* error_word() { return device_error_word(); }
 
 int device_sm_count() {
   int dev = 0;
@@ -79,6 +85,7 @@ const char* pkv_status_string(pkv_status status) {
     case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: shape not supported (block_size 16, head_dim 128, GQA 4)";
     case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: split-KV workspace missing or too small";
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA runtime call failed";
+    case PKV_ERR_EXHAUSTED: return "PKV_ERR_EXHAUSTED: not enough free blocks in the pool";
   }
   return "unknown pkv_status";
 }
@@ -203,7 +210,6 @@ void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups
                       int32_t max_suffix_blocks, int32_t sm_count, int32_t* prefix_blocks_per_split,
                       int32_t* suffix_blocks_per_split) {
   if (sm_count <= 0) sm_count = device_sm_count();
-  const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
   // prefix pass: about a third of the SMs' worth of (group, split, head)
   // CTAs.  The suffix pass runs beside it and needs the rest: an SM holding a
   // tensor-core CTA has room for one decode CTA only, so many short prefix

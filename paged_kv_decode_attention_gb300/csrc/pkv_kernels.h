@@ -114,6 +114,13 @@ cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, int32_t grid_x, cudaStream
 // Members per cascade group: 16 requests x 4 heads = one 64-row tile.
 constexpr int kCascadeGroup = 16;
 
+// Device error word of the current device (PKV_DEVERR_* bits).
+unsigned int* device_error_word();
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                               const int32_t* src, const int32_t* dst, int32_t num_pairs, unsigned int* err,
+                               cudaStream_t stream);
+
 cudaError_t launch_attn_combine(void* out, float* out_lse, const float* part_o, const float* part_lse,
                                 int32_t num_rows, int32_t num_splits, cudaStream_t stream);
 

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_function():
 
 def test_status_strings():
     lib = pkv.lib()
-    for code in range(6):
+    for code in range(7):
         assert lib.pkv_status_string(code).startswith(b"PKV_")
 
 
