@@ -35,7 +35,7 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -53,6 +53,15 @@ def _bind(lib):
     lib.oracle_paged_attention.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
+    lib.oracle_quantize_q8_0_group.argtypes = [c_p, c_p, c_p]
+    lib.oracle_quantize_q8_0_group.restype = None
+    lib.oracle_kv_append_q8_0.argtypes = [c_p, c_p, i32, i32, i32, c_p, c_p, c_p, i32]
+    lib.oracle_kv_append_q8_0.restype = None
+    lib.oracle_dequantize_q8_0.argtypes = [c_p, c_p, i32, i32, i32]
+    lib.oracle_dequantize_q8_0.restype = None
+    lib.oracle_paged_attention_f64.argtypes = [c_p, c_p, c_p, c_p, c_p, i32, i32, i32, i32, c_p, i32, c_p, i32, i32,
+                                               i32, ctypes.c_double, i32]
+    lib.oracle_paged_attention_f64.restype = ctypes.c_int
     return lib
 
 
@@ -82,7 +91,8 @@ def build_variant(source_text: str, out_path: str) -> str:
     src = out_path + ".c"
     with open(src, "w") as f:
         f.write(source_text)
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", src, "-o", out_path, "-lm"],
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp", src, "-o", out_path,
+                    "-lm"],
                    check=True)
     return out_path
 
@@ -196,3 +206,62 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, src_blocks, dst_blocks
     for s, d in zip(src_blocks, dst_blocks):
         k_cache[int(d)] = k_cache[int(s)]
         v_cache[int(d)] = v_cache[int(s)]
+
+
+# ---------------------------------------------------------------------------
+# q8_0 KV (§8.4.2, Fig. 8-23): 32 values share one FP16 scale; 8-bit codes.
+# Pool per tensor: uint8 [num_blocks][Hkv][2176] = codes int8 [16][128] then
+# scales fp16 [16][4] for each (block, kv head).
+# ---------------------------------------------------------------------------
+Q8_TILE_BYTES = 2176
+
+
+def quantize_q8_0_group(x_bits: np.ndarray):
+    """32 BF16 bit patterns -> (int8 codes[32], uint16 FP16 scale bits)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    assert x.size == 32
+    codes = np.zeros(32, np.int8)
+    sb = np.zeros(1, np.uint16)
+    _load().oracle_quantize_q8_0_group(_ptr(x), _ptr(codes), _ptr(sb))
+    return codes, int(sb[0])
+
+
+def kv_append_q8_0(k_cache: np.ndarray, v_cache: np.ndarray, slot_mapping, k_new, v_new, block_size: int = 16):
+    """In place: quantize and store new K/V rows in q8_0 pools (uint8 [nb][Hkv][2176])."""
+    assert k_cache.dtype == np.uint8 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    nb, hkv, tb = k_cache.shape
+    assert tb == Q8_TILE_BYTES
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    _load().oracle_kv_append_q8_0(_ptr(k_cache), _ptr(v_cache), nb, block_size, hkv, _ptr(slot_mapping), _ptr(k_new),
+                                  _ptr(v_new), slot_mapping.shape[0])
+
+
+def dequantize_q8_0(cache: np.ndarray, block_size: int = 16) -> np.ndarray:
+    """q8_0 pool -> float64 [nb][Hkv][16][128] of scale * code."""
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    nb, hkv, _ = cache.shape
+    out = np.zeros((nb, hkv, block_size, 128), np.float64)
+    _load().oracle_dequantize_q8_0(_ptr(cache), _ptr(out), nb, hkv, block_size)
+    return out
+
+
+def paged_attention_f64(q, k_cache_f64, v_cache_f64, block_tables, context_lens, q_len: int, scale: float,
+                        num_threads: int = 0, with_lse: bool = False):
+    """Attention over float64 pools [nb][Hkv][16][D] (e.g. dequantized q8_0)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kc = np.ascontiguousarray(k_cache_f64, dtype=np.float64)
+    vc = np.ascontiguousarray(v_cache_f64, dtype=np.float64)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    b, ql, hq, d = q.shape
+    nb, hkv, bs, _ = kc.shape
+    out = np.zeros((b, q_len, hq, d), np.float64)
+    lse = np.zeros((b, q_len, hq), np.float64)
+    rc = _load().oracle_paged_attention_f64(_ptr(out), _ptr(lse), _ptr(q), _ptr(kc), _ptr(vc), nb, bs, hkv, d,
+                                            _ptr(tables), tables.shape[1], _ptr(ctx), b, q_len, hq, float(scale),
+                                            int(num_threads))
+    if rc != 0:
+        raise ValueError("block table entry outside the pool")
+    return (out, lse) if with_lse else out

@@ -172,3 +172,138 @@ int32_t oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/* ---------------------------------------------------------------------------
+ * q8_0 KV ("Chapter 8: Inference Optimization" §8.4.2, Fig. 8-23): every 32
+ * consecutive values of a token's head vector share one 2-byte scale and are
+ * stored as 8-bit codes, 34 bytes per 32 values.  The pages fix the storage;
+ * the rounding is the plain symmetric one: d = max|x| / 127 in FP32, code =
+ * round-half-away-from-zero(x * (1/d)), scale stored as FP16 (round to
+ * nearest even); value = fp16(d) * code.  The integer decisions are taken in
+ * FP32 exactly as written (the build disables contraction into FMA).
+ * Tile of one (block, kv head): codes int8 [16][128] then scales fp16 [16][4].
+ * --------------------------------------------------------------------------- */
+#define Q8_TILE_BYTES 2176
+
+static float bf16_float(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* 32 BF16 values -> 32 codes and the FP16 bit pattern of the scale. */
+void oracle_quantize_q8_0_group(const uint16_t* x, int8_t* codes, uint16_t* scale_bits) {
+  float amax = 0.0f;
+  for (int i = 0; i < 32; ++i) {
+    float a = fabsf(bf16_float(x[i]));
+    if (a > amax) amax = a;
+  }
+  float d = amax / 127.0f;
+  float id = d != 0.0f ? 1.0f / d : 0.0f;
+  for (int i = 0; i < 32; ++i) codes[i] = (int8_t)roundf(bf16_float(x[i]) * id);
+  _Float16 h = (_Float16)d;
+  memcpy(scale_bits, &h, sizeof h);
+}
+
+static double fp16_value(uint16_t bits) {
+  _Float16 h;
+  memcpy(&h, &bits, sizeof h);
+  return (double)(float)h;
+}
+
+/* Store each new token's K and V in its slot of q8_0 pools
+ * [num_blocks][num_kv_heads][Q8_TILE_BYTES]; same slot rules as
+ * oracle_kv_append. */
+void oracle_kv_append_q8_0(uint8_t* k_cache, uint8_t* v_cache, int32_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, const int64_t* slot_mapping, const uint16_t* k_new,
+                           const uint16_t* v_new, int32_t num_tokens) {
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= (int64_t)num_blocks * block_size) continue;
+    int64_t blk = slot / block_size;
+    int32_t off = (int32_t)(slot % block_size);
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      for (int which = 0; which < 2; ++which) {
+        uint8_t* tile = (which ? v_cache : k_cache) + (blk * num_kv_heads + h) * (int64_t)Q8_TILE_BYTES;
+        const uint16_t* src = (which ? v_new : k_new) + ((int64_t)t * num_kv_heads + h) * 128;
+        for (int g = 0; g < 4; ++g) {
+          uint16_t sb;
+          oracle_quantize_q8_0_group(src + 32 * g, (int8_t*)(tile + off * 128 + 32 * g), &sb);
+          memcpy(tile + 2048 + (off * 4 + g) * 2, &sb, 2);
+        }
+      }
+    }
+  }
+}
+
+/* Dequantize q8_0 pools into double pools [num_blocks][num_kv_heads][block_size][128]. */
+void oracle_dequantize_q8_0(const uint8_t* cache, double* out, int32_t num_blocks, int32_t num_kv_heads,
+                            int32_t block_size) {
+  for (int64_t bh = 0; bh < (int64_t)num_blocks * num_kv_heads; ++bh) {
+    const uint8_t* tile = cache + bh * Q8_TILE_BYTES;
+    for (int32_t t = 0; t < block_size; ++t)
+      for (int32_t d = 0; d < 128; ++d) {
+        uint16_t sb;
+        memcpy(&sb, tile + 2048 + (t * 4 + d / 32) * 2, 2);
+        out[(bh * block_size + t) * 128 + d] = fp16_value(sb) * (double)(int8_t)tile[t * 128 + d];
+      }
+  }
+}
+
+/* Attention over double pools (e.g. dequantized q8_0 values); otherwise
+ * exactly oracle_paged_attention. */
+int oracle_paged_attention_f64(double* out, double* out_lse, const uint16_t* q, const double* k_cache,
+                               const double* v_cache, int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                               int32_t head_dim, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                               double scale, int32_t num_threads) {
+  int32_t group = num_q_heads / num_kv_heads;
+  int64_t n_rows = (int64_t)num_seqs * q_len * num_q_heads;
+  for (int32_t r = 0; r < num_seqs; ++r)
+    for (int64_t j = 0; j * block_size < context_lens[r]; ++j) {
+      if (j >= max_blocks_per_seq) return -1;
+      int32_t blk = block_tables[(int64_t)r * max_blocks_per_seq + j];
+      if (blk < 0 || blk >= num_blocks) return -1;
+    }
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t row = 0; row < n_rows; ++row) {
+    int32_t h = (int32_t)(row % num_q_heads);
+    int32_t i = (int32_t)((row / num_q_heads) % q_len);
+    int32_t r = (int32_t)(row / ((int64_t)num_q_heads * q_len));
+    int32_t ctx = context_lens[r];
+    int32_t kvh = h / group;
+    const uint16_t* qv = q + (((int64_t)r * q_len + i) * num_q_heads + h) * head_dim;
+    double* o = out + row * head_dim;
+    for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+    double* logit = (double*)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+    double m = -INFINITY;
+    for (int64_t t = 0; t < ctx; ++t) {
+      if (!key_visible(t, ctx, q_len, i)) continue;
+      int64_t blk = block_tables[(int64_t)r * max_blocks_per_seq + t / block_size];
+      int32_t off = (int32_t)(t % block_size);
+      double dot = 0.0;
+      for (int32_t d = 0; d < head_dim; ++d)
+        dot += bf16_value(qv[d]) * k_cache[cache_index(blk, kvh, off, d, num_kv_heads, block_size, head_dim)];
+      logit[t] = scale * dot;
+      if (logit[t] > m) m = logit[t];
+    }
+    double denom = 0.0;
+    for (int64_t t = 0; t < ctx; ++t)
+      if (key_visible(t, ctx, q_len, i)) denom += exp(logit[t] - m);
+    for (int64_t t = 0; t < ctx; ++t) {
+      if (!key_visible(t, ctx, q_len, i)) continue;
+      int64_t blk = block_tables[(int64_t)r * max_blocks_per_seq + t / block_size];
+      int32_t off = (int32_t)(t % block_size);
+      double w = exp(logit[t] - m) / denom;
+      for (int32_t d = 0; d < head_dim; ++d)
+        o[d] += w * v_cache[cache_index(blk, kvh, off, d, num_kv_heads, block_size, head_dim)];
+    }
+    if (out_lse) out_lse[row] = denom > 0.0 ? m + log(denom) : -INFINITY;
+    free(logit);
+  }
+  return 0;
+}

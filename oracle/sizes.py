@@ -80,3 +80,25 @@ def step_read_bytes(weight_bytes: int, b: int, context: int, bytes_per_token: in
 def kv_dominance_batch(weight_bytes: int, context: int, bytes_per_token: int) -> int:
     """§8.2.1: smallest b whose KV reads reach the shared weight reads, ceil(D_w / (L k))."""
     return -(-weight_bytes // (context * bytes_per_token))
+
+
+def group_bytes(values: int, code_bits: int, scale_bytes: int = 2) -> float:
+    """§8.4.2, Fig. 8-23: a group of `values` numbers stores its codes at
+    `code_bits` each plus one scale of `scale_bytes`."""
+    return values * code_bits / 8 + scale_bytes
+
+
+def quantized_mib(bf16_mib: float, code_bits: int, group: int = 32) -> float:
+    """§8.4.2: the same values regrouped -- BF16 spends 2*group bytes per
+    group, the quantized format group_bytes(group, code_bits)."""
+    return bf16_mib * group_bytes(group, code_bits) / (2 * group)
+
+
+def bits_per_value(code_bits: int, group: int = 32, scale_bytes: int = 2) -> float:
+    """§8.4.2: average storage per value, the scale included."""
+    return group_bytes(group, code_bits, scale_bytes) * 8 / group
+
+
+def saved_time_s(delta_bytes: float, bandwidth_bytes_per_s: float, convert_s: float) -> float:
+    """§8.4.2: net time saved by reading fewer bytes, dT = dD / beta - T_c."""
+    return delta_bytes / bandwidth_bytes_per_s - convert_s

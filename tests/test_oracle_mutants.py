@@ -3,7 +3,8 @@
 Each mutant is a one-line edit of pkv_oracle.c of the kind a careless
 restatement might make (a dropped scale, an off-by-one causal rule, a wrong
 GQA group, a transposed cache index, a dropped normalisation, a wrong BF16
-decode, a wrong slot split).  The copy is compiled on the CPU and the pins of
+decode, a wrong slot split, and the q8_0 quantiser's scale, rounding and
+layout).  The copy is compiled on the CPU and the pins of
 test_oracle_attention / test_oracle_sizes are run against it.
 """
 import inspect
@@ -12,6 +13,7 @@ import pytest
 
 import oracle
 import test_oracle_attention as A
+import test_oracle_q8 as Q
 import test_oracle_sizes as S
 
 MUTANTS = {
@@ -27,12 +29,23 @@ MUTANTS = {
     # ignores the block table: logical block j read from physical block j
     "table_ignored": ("int64_t blk = block_tables[(int64_t)r * max_blocks_per_seq + t / block_size];",
                       "int64_t blk = t / block_size;"),
+    # q8_0 (§8.4.2): wrong code range, round-half-even, scale stored in the
+    # wrong slot, codes read unsigned, wrong group of a scale, groups stored
+    # in reverse, V read from the K pool
+    "q8_scale_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
+    "q8_round_half_even": ("codes[i] = (int8_t)roundf(", "codes[i] = (int8_t)rintf("),
+    "q8_scale_slot": ("memcpy(tile + 2048 + (off * 4 + g) * 2, &sb, 2);",
+                      "memcpy(tile + 2048 + (g * 16 + off) * 2, &sb, 2);"),
+    "q8_codes_unsigned": ("(double)(int8_t)tile[t * 128 + d]", "(double)tile[t * 128 + d]"),
+    "q8_scale_group": ("(t * 4 + d / 32) * 2", "(t * 4 + d / 64) * 2"),
+    "q8_groups_reversed": ("(int8_t*)(tile + off * 128 + 32 * g)", "(int8_t*)(tile + off * 128 + 32 * (3 - g))"),
+    "q8_attention_reads_k_as_v": ("o[d] += w * v_cache[cache_index(", "o[d] += w * k_cache[cache_index("),
 }
 
 
 def _pins():
     fns = []
-    for mod in (A, S):
+    for mod in (A, Q, S):
         for name, fn in inspect.getmembers(mod, inspect.isfunction):
             if name.startswith("test_") and fn.__module__ == mod.__name__:
                 fns.append((name, fn))
