@@ -13,7 +13,7 @@ block counts once), Q and output, the block-table entries and context
 lengths read, plus the append's read and write of the new tokens' K/V.
 
   python bench.py [--workload short|long|mixed|chunk|tiny] [--steps K] [--warmup W]
-                  [--kv-blocks-per-split S] [--graph] [--impl reference]
+                  [--kv bf16|q8_0] [--kv-blocks-per-split S] [--graph] [--impl reference]
 """
 from __future__ import annotations
 
@@ -67,14 +67,20 @@ WORKLOAD_TEXT = {
 }
 
 
-def bytes_per_layer(w):
+# q8_0 (§8.4.2): 34 bytes per 32 values instead of 64
+KV_BYTES_PER_TOKEN_Q8 = KV_BYTES_PER_TOKEN * 34 // 64
+
+
+def bytes_per_layer(w, kv: str = "bf16"):
     """(attention algorithmic bytes, append bytes) of one layer-call."""
+    stored = KV_BYTES_PER_TOKEN_Q8 if kv == "q8_0" else KV_BYTES_PER_TOKEN
     uniq = w.unique_tokens()
     qo = 2 * w.num_seqs * w.q_len * w.num_q_heads * w.head_dim * 2
     table = sum(-(-int(c) // 16) for c in w.context_lens) * 4 + w.num_seqs * 4
-    attn = uniq * KV_BYTES_PER_TOKEN + qo + table
+    attn = uniq * stored + qo + table
     t = int((w.slot_mapping >= 0).sum())
-    append = t * KV_BYTES_PER_TOKEN * 2 + w.slot_mapping.size * 8  # read new K/V, write slots, read slot ids
+    # read the new BF16 K/V, write them in the pool's format, read the slot ids
+    append = t * (KV_BYTES_PER_TOKEN + stored) + w.slot_mapping.size * 8
     return attn, append
 
 
@@ -194,6 +200,45 @@ def oracle_sample(w, kc_dev, vc_dev, max_seqs: int):
     return sub
 
 
+def oracle_sample_q8(w, kq_dev, vq_dev, max_seqs: int):
+    """oracle_sample for q8_0 pools: host copies of the q8_0 tiles the sampled requests read."""
+    seq_ids = list(range(min(max_seqs, w.num_seqs)))
+    need = {}
+    for r in seq_ids:
+        for b in w.block_tables[r, :-(-int(w.context_lens[r]) // 16)]:
+            need.setdefault(int(b), len(need))
+    ids = torch.tensor(sorted(need, key=need.get), dtype=torch.long, device=kq_dev.device)
+    kq = kq_dev.index_select(0, ids).cpu().numpy().copy()
+    vq = vq_dev.index_select(0, ids).cpu().numpy().copy()
+    tables = np.vectorize(lambda b: need.get(int(b), 0))(w.block_tables[seq_ids]).astype(np.int32)
+    sl = w.slot_mapping.reshape(w.num_seqs, w.q_len)[seq_ids].reshape(-1)
+    sl = np.array([need[int(s) // 16] * 16 + int(s) % 16 if s >= 0 else -1 for s in sl], np.int64)
+    sub = W.Workload(**{**w.__dict__, "k_cache": None, "v_cache": None, "block_tables": tables,
+                        "context_lens": w.context_lens[seq_ids].copy(), "q": w.q[seq_ids].copy(),
+                        "k_new": w.k_new.reshape(w.num_seqs, w.q_len, -1, 128)[seq_ids].reshape(-1, w.num_kv_heads, 128),
+                        "v_new": w.v_new.reshape(w.num_seqs, w.q_len, -1, 128)[seq_ids].reshape(-1, w.num_kv_heads, 128),
+                        "slot_mapping": sl})
+    return sub, kq, vq
+
+
+def time_oracle_q8(sub, kq, vq, budget_s: float = 12.0, max_reps: int = 200):
+    """The oracle's q8_0 append, dequantisation and FP64 attention on the sample."""
+    import oracle
+    attn_b, app_b = bytes_per_layer(sub, "q8_0")
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.kv_append_q8_0(kq, vq, sub.slot_mapping, sub.k_new, sub.v_new)
+        oracle.paged_attention_f64(sub.q, oracle.dequantize_q8_0(kq), oracle.dequantize_q8_0(vq), sub.block_tables,
+                                   sub.context_lens, 1, sub.scale)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    per = el / reps
+    return {"gbs": (attn_b + app_b) / per / 1e9, "s_per_layer_call": per, "reps": reps,
+            "cores": oracle.max_threads(), "seqs": sub.num_seqs}
+
+
 def time_oracle(sub, budget_s: float = 12.0, max_reps: int = 200):
     """Run the oracle's append + attention on the sample until ~budget_s; GB/s of algorithmic bytes."""
     import oracle
@@ -230,6 +275,8 @@ def main():
     ap.add_argument("--suffix-blocks-per-split", type=int, default=0, help="cascade suffix pass split (0 = plan)")
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workloads: plain paged attention instead of the cascade call")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "q8_0"],
+                    help="KV pool format: bf16, or q8_0 (decode only; tensor-core dequantising kernel)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -249,7 +296,10 @@ def main():
     w, layers = make_workload(args.workload, args.seed, args.num_seqs)
     if args.layers > 0:
         layers = args.layers
-    attn_b, app_b = bytes_per_layer(w)
+    q8 = args.kv == "q8_0"
+    if q8 and w.q_len != 1:
+        raise SystemExit("--kv q8_0 is a decode (q_len 1) path")
+    attn_b, app_b = bytes_per_layer(w, args.kv)
     step_bytes = layers * (attn_b + app_b)
     tokens_layers = int(w.context_lens.sum()) * w.q_len * layers if w.q_len > 1 else int(w.context_lens.sum()) * layers
 
@@ -263,17 +313,36 @@ def main():
     lib = pkv.lib()
     b, ql, hq, hkv, d = w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim
     maxb = w.max_blocks_per_seq
-    bps = args.kv_blocks_per_split or pkv.choose_kv_blocks_per_split(b, hkv, ql, maxb)
+    if q8:
+        bps = args.kv_blocks_per_split or pkv.choose_kv_blocks_per_split_q8_0(b, hkv, maxb)
+    else:
+        bps = args.kv_blocks_per_split or pkv.choose_kv_blocks_per_split(b, hkv, ql, maxb)
     bps = min(bps, maxb)
     splits = -(-maxb // bps)
 
     # device state: per-layer pools (filled on the device), per-layer step inputs/outputs
-    pool_shape = (layers, w.num_blocks, hkv, 16, d)
-    k_pool = torch.empty(pool_shape, dtype=torch.bfloat16, device=dev)
-    v_pool = torch.empty(pool_shape, dtype=torch.bfloat16, device=dev)
-    for l in range(layers):
-        W.fill_pool_device(k_pool[l], 1000 + 2 * l + args.seed * 7919)
-        W.fill_pool_device(v_pool[l], 1001 + 2 * l + args.seed * 7919)
+    if q8:
+        # BF16 values drawn on the device, quantised into each layer's q8_0 pool by the library's append
+        k_pool = torch.empty((layers, w.num_blocks, hkv, pkv.Q8_TILE_BYTES), dtype=torch.uint8, device=dev)
+        v_pool = torch.empty_like(k_pool)
+        tmp_k = torch.empty((w.num_blocks, hkv, 16, d), dtype=torch.bfloat16, device=dev)
+        tmp_v = torch.empty_like(tmp_k)
+        all_slots = torch.arange(w.num_blocks * 16, dtype=torch.int64, device=dev)
+        tok = lambda p: p.permute(0, 2, 1, 3).contiguous().view(w.num_blocks * 16, hkv, d)
+        for l in range(layers):
+            W.fill_pool_device(tmp_k, 1000 + 2 * l + args.seed * 7919)
+            W.fill_pool_device(tmp_v, 1001 + 2 * l + args.seed * 7919)
+            pkv.kv_append_q8_0(k_pool[l], v_pool[l], all_slots, tok(tmp_k), tok(tmp_v))
+        del tmp_k, tmp_v, all_slots
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    else:
+        pool_shape = (layers, w.num_blocks, hkv, 16, d)
+        k_pool = torch.empty(pool_shape, dtype=torch.bfloat16, device=dev)
+        v_pool = torch.empty(pool_shape, dtype=torch.bfloat16, device=dev)
+        for l in range(layers):
+            W.fill_pool_device(k_pool[l], 1000 + 2 * l + args.seed * 7919)
+            W.fill_pool_device(v_pool[l], 1001 + 2 * l + args.seed * 7919)
     rng = np.random.Generator(np.random.PCG64(args.seed + 17))
     t_tok = w.slot_mapping.size
     h_q = torch.from_numpy(W.randn_bf16(rng, (layers, b, ql, hq, d))).view(torch.bfloat16)
@@ -289,19 +358,19 @@ def main():
     kn, vn = h_kn.to(dev), h_vn.to(dev)
     tables, ctx, slots = h_tables.to(dev), h_ctx.to(dev), h_slots.to(dev)
     out = torch.empty_like(q)
-    ws_bytes = pkv.workspace_size(b, ql, hq, maxb, bps)
+    ws_bytes = pkv.workspace_size_q8_0(b, hq, maxb, bps) if q8 else pkv.workspace_size(b, ql, hq, maxb, bps)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     desc = pkv.CacheDesc(w.num_blocks, 16, hkv, d)
     stream = torch.cuda.Stream(dev)  # non-default: CUDA graphs can be captured on it
     torch.cuda.set_stream(stream)
     sp = stream.cuda_stream
-    pool_stride = w.num_blocks * hkv * 16 * d * 2
+    pool_stride = w.num_blocks * hkv * (pkv.Q8_TILE_BYTES if q8 else 16 * d * 2)
     kp0, vp0 = k_pool.data_ptr(), v_pool.data_ptr()
     q_stride, kn_stride = b * ql * hq * d * 2, t_tok * hkv * d * 2
-    launches_per_layer = 1 + 1 + (1 if splits > 1 else 0)
+    launches_per_layer = 1 + 1 + (1 if (splits > 8 or (splits > 1 and (ql >= 16 or q8))) else 0)
     # shared prefixes: the caller states the groups and the cascade call reads each prefix once per group
     gs_h, gb_h, sp_h = W.prefix_groups(w)
-    cascade = (not args.no_cascade) and gs_h.shape[0] > 0 and ql == 1
+    cascade = (not args.no_cascade) and gs_h.shape[0] > 0 and ql == 1 and not q8
     if cascade:
         maxp = int(gb_h.max())
         maxs = W.max_suffix_blocks(w, sp_h)
@@ -319,12 +388,17 @@ def main():
             raise RuntimeError(f"{what}: {lib.pkv_status_string(st).decode()}")
 
     def layer_call(l, ev=None):
-        check(lib.pkv_kv_append(kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc), slots.data_ptr(),
-                                kn.data_ptr() + l * kn_stride, vn.data_ptr() + l * kn_stride, t_tok, sp),
-              "kv_append")
+        append = lib.pkv_kv_append_q8_0 if q8 else lib.pkv_kv_append
+        check(append(kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc), slots.data_ptr(),
+                     kn.data_ptr() + l * kn_stride, vn.data_ptr() + l * kn_stride, t_tok, sp), "kv_append")
         if ev is not None:
             ev[0].record(stream)
-        if cascade:
+        if q8:
+            check(lib.pkv_paged_attention_q8_0(out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride,
+                                               kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc),
+                                               tables.data_ptr(), maxb, ctx.data_ptr(), b, hq, w.scale, bps,
+                                               ws.data_ptr(), ws.numel(), sp), "paged_attention_q8_0")
+        elif cascade:
             check(lib.pkv_paged_attention_cascade(
                 out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride, kp0 + l * pool_stride,
                 vp0 + l * pool_stride, ctypes.byref(desc), tables.data_ptr(), maxb, ctx.data_ptr(), b, hq, w.scale,
@@ -404,6 +478,11 @@ def main():
             for dst, src in ((q, p_q), (kn, p_kn), (vn, p_vn), (tables, p_tables), (ctx, p_ctx), (slots, p_slots)):
                 dst.copy_(src, non_blocking=True)
             for l in range(layers):
+                if q8:
+                    pkv.kv_append_q8_0(k_pool[l], v_pool[l], slots, kn[l], vn[l])
+                    pkv.paged_attention_q8_0(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, w.scale,
+                                             kv_blocks_per_split=bps, workspace=ws)
+                    continue
                 pkv.kv_append(k_pool[l], v_pool[l], slots, kn[l], vn[l])
                 if cascade:
                     pkv.paged_attention_cascade(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, w.scale, gs_d, gb_d,
@@ -428,8 +507,12 @@ def main():
     # ---- CPU oracle baseline (rank 0 at N=1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sub = oracle_sample(w, k_pool[0], v_pool[0], max_seqs=w.num_seqs)
-        r = time_oracle(sub, budget_s=args.oracle_budget_s)
+        if q8:
+            sub, kq_h, vq_h = oracle_sample_q8(w, k_pool[0], v_pool[0], max_seqs=w.num_seqs)
+            r = time_oracle_q8(sub, kq_h, vq_h, budget_s=args.oracle_budget_s)
+        else:
+            sub = oracle_sample(w, k_pool[0], v_pool[0], max_seqs=w.num_seqs)
+            r = time_oracle(sub, budget_s=args.oracle_budget_s)
         cpu = {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
                "sample": f"layer 0 of this workload ({r['seqs']} requests, append + attention), FP64 C oracle, "
                          f"{r['reps']} repetitions, {r['s_per_layer_call'] * 1e3:.1f} ms per layer-call"}
@@ -449,22 +532,24 @@ def main():
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
-        tj = json.load(open(tpath)).get(args.workload)
+        tj = json.load(open(tpath)).get(args.workload + ("_q8_0" if q8 else ""))
         if tj and tj.get("kernel_build") == kernel_build_id():
             traffic = tj.get("bytes_per_launch")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "q8_0 KV, f16 tensor-core products, f32 softmax" if q8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_seqs": b, "q_len": ql,
                    "layers": layers, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16,
                    "ctx_min": int(w.context_lens.min()), "ctx_max": int(w.context_lens.max()),
+                   "kv_format": args.kv,
                    "kv_blocks_per_split": bps, "splits": splits, "cuda_graph": bool(graph is not None),
                    "cascade": ({"groups": int(gs_h.shape[0]), "prefix_blocks": maxp, "max_suffix_blocks": maxs,
                                 "prefix_blocks_per_split": pbps,
                                 "suffix_blocks_per_split": sbps} if cascade else None),
                    "l2": "inputs larger than L2: one KV pool per layer, %.1f GB total" % (
-                       2 * k_pool.numel() * 2 / 1e9),
+                       2 * k_pool.numel() * k_pool.element_size() / 1e9),
                    "parallelism": f"replicas x{world}"},
         "us_per_layer_call": round(attn_us, 3),
         "attention_tokens_layers_per_s": round(world * tokens_layers / (ms_per_step * 1e-3), 1),
@@ -472,7 +557,9 @@ def main():
         "bytes_per_step": int(step_bytes),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
-                     "kernel": ("paged_attention_cascade call (prefix tensor-core pass + suffix decode + combine)"
+                     "kernel": ("paged_attention_q8_0 call (tensor-core q8_0 decode%s)" % (
+                                    " + combine" if splits > 1 else "") if q8 else
+                                "paged_attention_cascade call (prefix tensor-core pass + suffix decode + combine)"
                                 if cascade else "paged_attention call (%s%s)" % (
                                     "tensor-core chunk" if ql >= 16 else "decode",
                                     " + combine" if (splits > 8 or (ql >= 16 and splits > 1)) else "")),

@@ -323,6 +323,69 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
                            const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
                            void* stream);
 
+/*
+ * ---------------------------------------------------------------------------
+ * q8_0 KV cache (§8.4.2 "KV compression and read cost", Fig. 8-23): every 32
+ * consecutive values of a token's head vector share one 2-byte scale and keep
+ * 8-bit codes, 34 bytes instead of 64.  The page fixes the storage; this
+ * library quantises with the plain symmetric rule, in FP32 with IEEE
+ * rounding at every step:  d = max|x| / 127,  code = round-half-away-from-
+ * zero(x * (1/d))  (0 when d = 0),  scale = FP16(d) (round to nearest even),
+ * value = scale * code.  Inputs must be finite.
+ *
+ * Pool layout, per tensor: uint8 [num_blocks][num_kv_heads][PKV_Q8_TILE_BYTES];
+ * one (block, kv head) tile is int8 codes [16 tokens][128 dims] (token-major)
+ * followed by FP16 scales [16 tokens][4 groups] (group g = dims 32g..32g+31).
+ * `cache` describes the geometry exactly as for BF16 pools.
+ * ---------------------------------------------------------------------------
+ */
+#define PKV_Q8_TILE_BYTES 2176u
+
+/*
+ * pkv_kv_append_q8_0 -- pkv_kv_append for q8_0 pools: quantise each new
+ * token's K and V (BF16 [num_tokens][num_kv_heads][128], 16-byte aligned) and
+ * store codes and scales in its slot.  Same slot rules and errors as
+ * pkv_kv_append.  Deterministic: the same bits as any IEEE FP32 evaluation of
+ * the rule above.
+ */
+pkv_status pkv_kv_append_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                              const int64_t* slot_mapping, const void* k_new, const void* v_new, int32_t num_tokens,
+                              void* stream);
+
+/*
+ * pkv_choose_kv_blocks_per_split_q8_0 -- blocks per split for
+ * pkv_paged_attention_q8_0: its kernel keeps one persistent CTA per SM, so
+ * the split count is the one that best balances (request, KV head, split)
+ * units over sm_count CTAs (0 = current device), in whole 8-block tiles.
+ */
+int32_t pkv_choose_kv_blocks_per_split_q8_0(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
+                                            int32_t sm_count);
+
+/* Workspace bytes pkv_paged_attention_q8_0 needs (0 when there is one split). */
+size_t pkv_workspace_size_q8_0(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                               int32_t kv_blocks_per_split);
+
+/*
+ * pkv_paged_attention_q8_0 -- pkv_paged_attention for one decode step
+ * (q_len 1) over q8_0 pools: out = softmax(scale * q . K^T) V with K and V
+ * the dequantised values (scale * code).  q, out: BF16 [num_seqs][num_q_heads]
+ * [128].  kv_blocks_per_split 0 = pkv_choose_kv_blocks_per_split_q8_0; with
+ * more than one split, partials go to `workspace` (256-byte aligned,
+ * pkv_workspace_size_q8_0 bytes) and are merged by the combine kernel on the
+ * same stream.  Queries are scaled by a power of two into FP16 range, so any
+ * finite BF16 query is accepted.  Errors as pkv_paged_attention.
+ */
+pkv_status pkv_paged_attention_q8_0(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                    const pkv_cache_desc* cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                    int32_t num_q_heads, float scale, int32_t kv_blocks_per_split, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/* pkv_copy_blocks for q8_0 pools (num_kv_heads * PKV_Q8_TILE_BYTES per block). */
+pkv_status pkv_copy_blocks_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                                void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* pkv_status_string(pkv_status status);
 

@@ -33,7 +33,7 @@ bool valid_block(const pkv_block_pool* p, int32_t b) {
 }
 
 // One thread moves 16 bytes; a CTA moves one block of one tensor (K or V),
-// i.e. all KV heads of that block: num_kv_heads * 16 * 128 BF16 contiguous.
+// i.e. all KV heads of that block, contiguous (BF16 or q8_0 tiles alike).
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                                           int32_t num_blocks, int32_t chunks_per_block,
                                                           const int32_t* __restrict__ src,
@@ -55,11 +55,11 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_
 
 }  // namespace
 
-cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int64_t block_bytes,
                                const int32_t* src, const int32_t* dst, int32_t num_pairs, unsigned int* err,
                                cudaStream_t stream) {
   if (num_pairs == 0) return cudaSuccess;
-  const int32_t chunks = num_kv_heads * kBlockSize * kHeadDim * 2 / 16;
+  const int32_t chunks = static_cast<int32_t>(block_bytes / 16);
   return launch_pdl(copy_blocks_kernel, dim3(static_cast<unsigned>(num_pairs) * 2), dim3(256), 0, stream, 1,
                     static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks, chunks, src, dst, err);
 }
@@ -187,8 +187,26 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
   if (!k_cache || !v_cache || !src_blocks || !dst_blocks) return PKV_ERR_NULL;
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15) return PKV_ERR_UNSUPPORTED;
   if (num_pairs > (1 << 30)) return PKV_ERR_UNSUPPORTED;
-  return launch_copy_blocks(k_cache, v_cache, cache->num_blocks, cache->num_kv_heads, src_blocks, dst_blocks, num_pairs,
+  return launch_copy_blocks(k_cache, v_cache, cache->num_blocks,
+                            static_cast<int64_t>(cache->num_kv_heads) * kTileBytes, src_blocks, dst_blocks, num_pairs,
                             device_error_word(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                                void* stream) {
+  if (cache == nullptr) return PKV_ERR_NULL;
+  if (cache->num_blocks < 0 || cache->num_kv_heads <= 0 || num_pairs < 0) return PKV_ERR_SHAPE;
+  if (cache->block_size != kBlockSize || cache->head_dim != kHeadDim) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_blocks || !dst_blocks) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs > (1 << 30)) return PKV_ERR_UNSUPPORTED;
+  return launch_copy_blocks(k_cache, v_cache, cache->num_blocks,
+                            static_cast<int64_t>(cache->num_kv_heads) * kQ8TileBytes, src_blocks, dst_blocks,
+                            num_pairs, device_error_word(), static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
 }

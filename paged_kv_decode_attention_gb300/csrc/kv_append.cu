@@ -7,7 +7,10 @@
 // One thread moves 16 bytes; consecutive threads cover consecutive 16-byte
 // chunks of one (token, kv head) row of 256 bytes, so both the read of
 // k_new/v_new and the write into the 4 KiB cache tile are coalesced.  The
-// copy is a bit copy.
+// copy is a bit copy.  The q8_0 variant quantises each 32-value group on
+// the way in.
+#include <cuda_fp16.h>
+
 #include "pkv_common.cuh"
 #include "pkv_kernels.h"
 
@@ -50,7 +53,72 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
   }
 }
 
+// q8_0 append ("Chapter 8: Inference Optimization" §8.4.2, Fig. 8-23): one
+// warp per (token, kv head, K|V) row of 128 values; lane l holds values
+// 4l..4l+3, so lanes 8g..8g+7 hold group g.  Per group: d = max|x| / 127,
+// code = round-half-away(x * (1/d)), scale stored as FP16 (round to nearest
+// even).  Every step is one IEEE-rounded FP32 operation, so the codes and
+// scales are the same bits a CPU computes with the same operations.
+__global__ void __launch_bounds__(256) kv_append_q8_kernel(uint8_t* __restrict__ k_cache,
+                                                           uint8_t* __restrict__ v_cache, int64_t pool_slots,
+                                                           int32_t num_kv_heads,
+                                                           const int64_t* __restrict__ slot_mapping,
+                                                           const uint2* __restrict__ k_new,
+                                                           const uint2* __restrict__ v_new, int64_t rows,
+                                                           unsigned int* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t item = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; item < rows;
+       item += warps) {
+    // item = (t * 2 + which) * Hkv + h
+    const int h = static_cast<int>(item % num_kv_heads);
+    const int64_t rest = item / num_kv_heads;
+    const int which = static_cast<int>(rest & 1);
+    const int64_t t = rest >> 1;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= pool_slots) {
+      if (lane == 0 && h == 0 && which == 0) report(err, PKV_DEVERR_SLOT);
+      continue;
+    }
+    const uint2 w = (which ? v_new : k_new)[(t * num_kv_heads + h) * (kHeadDim / 4) + lane];
+    const float x0 = bf16_lo(w.x), x1 = bf16_hi(w.x), x2 = bf16_lo(w.y), x3 = bf16_hi(w.y);
+    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    const int c0 = static_cast<int>(roundf(__fmul_rn(x0, id)));
+    const int c1 = static_cast<int>(roundf(__fmul_rn(x1, id)));
+    const int c2 = static_cast<int>(roundf(__fmul_rn(x2, id)));
+    const int c3 = static_cast<int>(roundf(__fmul_rn(x3, id)));
+    const uint32_t codes = (static_cast<uint32_t>(c0) & 0xffu) | ((static_cast<uint32_t>(c1) & 0xffu) << 8) |
+                           ((static_cast<uint32_t>(c2) & 0xffu) << 16) | (static_cast<uint32_t>(c3) << 24);
+    const int64_t blk = slot / kBlockSize;
+    const int off = static_cast<int>(slot % kBlockSize);
+    uint8_t* tile = (which ? v_cache : k_cache) + (blk * num_kv_heads + h) * kQ8TileBytes;
+    *reinterpret_cast<uint32_t*>(tile + off * kHeadDim + lane * 4) = codes;
+    if ((lane & 7) == 0)
+      *reinterpret_cast<__half*>(tile + kQ8CodeBytes + (off * 4 + (lane >> 3)) * 2) = __float2half_rn(d);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_append_q8(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                                const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                                int32_t num_tokens, unsigned int* err, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(num_tokens) * 2 * num_kv_heads;
+  if (rows == 0) return cudaSuccess;
+  int64_t blocks = (rows + 7) / 8;  // 8 warps per CTA
+  if (blocks > 65536) blocks = 65536;
+  return launch_pdl(kv_append_q8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1,
+                    static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
+                    static_cast<int64_t>(num_blocks) * kBlockSize, num_kv_heads, slot_mapping,
+                    static_cast<const uint2*>(k_new), static_cast<const uint2*>(v_new), rows, err);
+}
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
                              const int64_t* slot_mapping, const void* k_new, const void* v_new,

@@ -345,6 +345,118 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
   return PKV_OK;
 }
 
+pkv_status pkv_kv_append_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                              const int64_t* slot_mapping, const void* k_new, const void* v_new, int32_t num_tokens,
+                              void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !slot_mapping || !k_new || !v_new) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return PKV_ERR_UNSUPPORTED;
+  return launch_kv_append_q8(k_cache, v_cache, cache->num_blocks, cache->num_kv_heads, slot_mapping, k_new, v_new,
+                             num_tokens, error_word(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+int32_t pkv_choose_kv_blocks_per_split_q8_0(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
+                                            int32_t sm_count) {
+  if (max_blocks_per_seq <= 0) return 1;
+  if (sm_count <= 0) sm_count = device_sm_count();
+  const int64_t rows = static_cast<int64_t>(num_seqs > 0 ? num_seqs : 1) * (num_kv_heads > 0 ? num_kv_heads : 1);
+  // Makespan of the persistent grid in 8-block tiles: the busiest CTA runs
+  // ceil(units / SMs) units; each unit costs its tiles plus about one tile of
+  // pipeline fill and epilogue, and splitting adds the combine pass.
+  int32_t best = max_blocks_per_seq;
+  int64_t best_cost = INT64_MAX;
+  for (int32_t splits = 1; splits <= 64; ++splits) {
+    int32_t bps = (max_blocks_per_seq + splits - 1) / splits;
+    bps = (bps + 7) / 8 * 8;
+    if (splits > 1 && bps < 16) break;
+    if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
+    const int64_t s_eff = (max_blocks_per_seq + bps - 1) / bps;
+    const int64_t units = rows * s_eff;
+    const int64_t per_cta = (units + sm_count - 1) / sm_count;
+    const int64_t cost = per_cta * ((bps + 7) / 8 + 1) + (s_eff > 1 ? 2 : 0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bps;
+    }
+  }
+  return best;
+}
+
+size_t pkv_workspace_size_q8_0(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                               int32_t kv_blocks_per_split) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || kv_blocks_per_split <= 0 ||
+      kv_blocks_per_split >= max_blocks_per_seq)
+    return 0;
+  const size_t splits = (static_cast<size_t>(max_blocks_per_seq) + kv_blocks_per_split - 1) / kv_blocks_per_split;
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
+  return align_up(rows * splits * kHeadDim * sizeof(float), 256) + align_up(rows * splits * sizeof(float), 256);
+}
+
+pkv_status pkv_paged_attention_q8_0(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                    const pkv_cache_desc* cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                    int32_t num_q_heads, float scale, int32_t kv_blocks_per_split, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_blocks_per_seq < 1 || kv_blocks_per_split < 0) return PKV_ERR_SHAPE;
+  if (num_q_heads != kGroup * cache->num_kv_heads) return PKV_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return PKV_ERR_SHAPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks_per_seq) * kBlockSize > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+  int32_t bps = kv_blocks_per_split;
+  if (bps == 0) bps = pkv_choose_kv_blocks_per_split_q8_0(num_seqs, cache->num_kv_heads, max_blocks_per_seq, 0);
+  if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
+  const int32_t splits = (max_blocks_per_seq + bps - 1) / bps;
+  const int64_t units = static_cast<int64_t>(num_seqs) * cache->num_kv_heads * splits;
+  if (units > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+
+  DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.err = error_word();
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = cache->num_blocks;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.num_seqs = num_seqs;
+  a.q_len = 1;
+  a.blocks_per_split = bps;
+  a.num_splits = splits;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.part_slots = splits;
+  const int sms = device_sm_count();
+  const int32_t grid = static_cast<int32_t>(units < sms ? units : sms);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (splits == 1) return launch_paged_decode_q8(a, grid, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  const size_t need = pkv_workspace_size_q8_0(num_seqs, num_q_heads, max_blocks_per_seq, bps);
+  if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        align_up(rows * splits * kHeadDim * sizeof(float), 256));
+  if (launch_paged_decode_q8(a, grid, s) != cudaSuccess) return PKV_ERR_CUDA;
+  return launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), splits, s) ==
+                 cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_attn_combine(void* out, float* out_lse, const float* partial_o, const float* partial_lse,
                             int32_t num_rows, int32_t head_dim, int32_t num_splits, void* stream) {
   if (num_rows < 0 || num_splits < 1) return PKV_ERR_SHAPE;

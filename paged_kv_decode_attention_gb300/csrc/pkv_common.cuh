@@ -18,6 +18,10 @@ constexpr int kBlockSize = 16;                       // tokens per physical bloc
 constexpr int kHeadDim = 128;                        // dims per head
 constexpr int kGroup = 4;                            // query heads per KV head
 constexpr int kTileBytes = kBlockSize * kHeadDim * 2;  // one (block, kv head) tile: 4 KiB
+// q8_0 tile of one (block, kv head): int8 codes [16][128], then the FP16
+// scale of every 32-value group, [16][4]: 64 groups of 34 bytes.
+constexpr int kQ8CodeBytes = kBlockSize * kHeadDim;                  // 2048
+constexpr int kQ8TileBytes = kQ8CodeBytes + kBlockSize * kHeadDim / 32 * 2;  // 2176
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s: a healthy wait takes microseconds
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -53,6 +57,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Non-blocking test of the same condition (for a thread that polls several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
       : "r"(smem_addr(bar)), "r"(parity)

@@ -114,10 +114,20 @@ cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, int32_t grid_x, cudaStream
 // Members per cascade group: 16 requests x 4 heads = one 64-row tile.
 constexpr int kCascadeGroup = 16;
 
+// q8_0 KV (pools of kQ8TileBytes per (block, kv head)): quantising append,
+// and decode (q_len 1) on tensor cores, `grid` persistent CTAs walking the
+// (request, KV head, split) units; num_splits > 1 writes workspace partials.
+cudaError_t launch_kv_append_q8(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                                const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                                int32_t num_tokens, unsigned int* err, cudaStream_t stream);
+cudaError_t launch_paged_decode_q8(const DecodeArgs& a, int32_t grid, cudaStream_t stream);
+
 // Device error word of the current device (PKV_DEVERR_* bits).
 unsigned int* device_error_word();
 
-cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+// Copies whole blocks (all KV heads) of both pools; block_bytes per block,
+// a multiple of 16.
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int32_t num_blocks, int64_t block_bytes,
                                const int32_t* src, const int32_t* dst, int32_t num_pairs, unsigned int* err,
                                cudaStream_t stream);
 

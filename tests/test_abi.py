@@ -113,3 +113,46 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         pkv.kv_append(x, x, torch.zeros(1, dtype=torch.int64), torch.zeros(1, 8, 128, dtype=torch.bfloat16),
                       torch.zeros(1, 8, 128, dtype=torch.bfloat16))
+
+
+def test_q8_split_heuristic_and_workspace_are_host_arithmetic():
+    lib = pkv.lib()
+    # 37 requests x 8 KV heads = 296 units on 152 SMs: two units per CTA, no split
+    assert lib.pkv_choose_kv_blocks_per_split_q8_0(37, 8, 144, 152) == 144
+    # few long rows: split into whole 8-block tiles, at least 16 blocks each
+    bps = lib.pkv_choose_kv_blocks_per_split_q8_0(2, 8, 528, 152)
+    assert 16 <= bps < 528 and bps % 8 == 0
+    assert lib.pkv_workspace_size_q8_0(37, 32, 144, 144) == 0
+    rows, splits = 2 * 32, -(-528 // bps)
+    o_bytes = -(-rows * splits * 128 * 4 // 256) * 256
+    l_bytes = -(-rows * splits * 4 // 256) * 256
+    assert lib.pkv_workspace_size_q8_0(2, 32, 528, bps) == o_bytes + l_bytes
+
+
+def test_q8_argument_errors():
+    lib = pkv.lib()
+    p = ctypes.c_void_p(256)
+    d = ctypes.byref(_desc())
+    assert lib.pkv_kv_append_q8_0(p, p, None, p, p, p, 1, None) == 1
+    assert lib.pkv_kv_append_q8_0(p, p, ctypes.byref(_desc(head_dim=64)), p, p, p, 1, None) == 3
+    assert lib.pkv_kv_append_q8_0(p, p, d, p, p, p, -1, None) == 2
+    assert lib.pkv_kv_append_q8_0(p, p, d, p, ctypes.c_void_p(264), p, 1, None) == 3  # k_new misaligned
+    assert lib.pkv_kv_append_q8_0(p, p, d, p, p, p, 0, None) == 0
+
+    def call(**kw):
+        a = dict(out=p, q=p, k=p, v=p, desc=d, bt=p, maxb=64, cl=p, b=2, hq=32, scale=0.1, bps=16, ws=None, wsb=0)
+        a.update(kw)
+        return lib.pkv_paged_attention_q8_0(a["out"], a["q"], a["k"], a["v"], a["desc"], a["bt"], a["maxb"],
+                                            a["cl"], a["b"], a["hq"], a["scale"], a["bps"], a["ws"], a["wsb"], None)
+
+    assert call(desc=None) == 1
+    assert call(v=None) == 1
+    assert call(hq=8) == 3
+    assert call(maxb=0) == 2
+    assert call(scale=float("inf")) == 2
+    assert call(k=ctypes.c_void_p(260)) == 3
+    assert call() == 4                      # 4 splits need a workspace
+    assert call(ws=ctypes.c_void_p(256), wsb=16) == 4
+    assert call(b=0) == 0
+    assert lib.pkv_copy_blocks_q8_0(p, p, ctypes.byref(_desc(block_size=8)), p, p, 1, None) == 3
+    assert lib.pkv_copy_blocks_q8_0(p, p, d, p, p, 0, None) == 0
