@@ -22,22 +22,27 @@
 //   O += P' . V_codes      on the FP32 pipes (~4 cycles per token): P' = p * sV
 //        per (token, head, group), codes converted exactly to FP32.
 //
-// CTA = 15 warps, one per SM, persistent: it walks work units u = blockIdx.x,
-// + gridDim.x, ... (a unit is one (request, KV head, split)).
-//   warps 0-1: producers.  Per 128-token tile, warp 0 copies 8 blocks' K
-//              tiles (2176 B each) into a 4-stage K ring and warp 1 their V
-//              tiles into a 4-stage V ring, the latter once the tile's K has
+// CTA = 15 warps (17 with four producers), one per SM, persistent: it walks
+// work units u = blockIdx.x, + gridDim.x, ... (a unit is one (request, KV
+// head, split)).
+//   producers (warps 0-1, or 0-3): per 128-token tile, a K producer copies 8
+//              blocks' K tiles (2176 B each) into the K ring and a V producer
+//              their V tiles into the V ring, the latter once the tile's K has
 //              landed; one bulk copy per lane.
-//   warp 2   : MMA issuer (one thread): QK(i) into a double-buffered S in
+//   next warp: MMA issuer (one thread): QK(i) into a double-buffered S in
 //              tensor memory.
-//   warps 3-10: attention.  The two warps on TMEM sub-partition w read the S
-//              rows of tokens 32w .. 32w+31 (thread = token) and take 16 of them
-//              each; every warp keeps its own online-softmax state (max, sum,
-//              O for 4 heads x 128 dims, lane = 4 dims) and the eight states
-//              merge once per unit (log-sum-exp), so no tile needs a
-//              cross-warp exchange.
-//   warps 11-14: dequantisation of the ring's K codes into a double-buffered
-//              FP16 operand tile (128-byte swizzled rows), and the unit's Qbd.
+//   next 8   : attention, two groups of four that take alternate tiles.  In
+//              a group, warp w (TMEM sub-partition w) owns tokens 32w .. 32w+31
+//              of its tiles (thread = token for S) and keeps its own
+//              online-softmax state (max, sum, O for 4 heads x 128 dims, lane =
+//              4 dims); the eight states merge once per unit (log-sum-exp), so
+//              no tile needs a cross-warp exchange.  The weights are taken
+//              against a maximum that moves only when a score exceeds it by
+//              more than 2^8, so most tiles skip the warp-wide reduction.
+//   last 4   : dequantisation of the ring's K codes into a double-buffered
+//              FP16 operand tile (128-byte swizzled rows), the unit's Qbd, and
+//              a copy of the tile's K scales for the softmax, so that a K stage
+//              is free as soon as its codes are converted.
 // Every wait is bounded (about 2 s) and reports PKV_DEVERR_TIMEOUT instead of
 // hanging; the roles exchange data only through mbarriers.
 #include <cmath>
@@ -58,37 +63,45 @@ namespace {
 #endif
 constexpr int kKStages = PKV_Q8_K_STAGES;
 constexpr int kVStages = PKV_Q8_V_STAGES;
-constexpr int kProducerWarps = 2;
-constexpr int kMmaWarp = kProducerWarps;                          // 2
-constexpr int kFirstAttnWarp = kMmaWarp + 1;                    // 3
+#ifndef PKV_Q8_PRODUCERS
+#define PKV_Q8_PRODUCERS 2
+#endif
+constexpr int kProducerWarps = PKV_Q8_PRODUCERS;  // half for the K ring, half for the V ring
+constexpr int kPerRing = kProducerWarps / 2;     // warps per ring, taking tiles in turn
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kFirstAttnWarp = kMmaWarp + 1;
 constexpr int kAttnWarps = 8;
-constexpr int kFirstDqWarp = kFirstAttnWarp + kAttnWarps;       // 11
-constexpr int kQ8Threads = (kFirstDqWarp + 4) * 32;             // 480
+constexpr int kFirstDqWarp = kFirstAttnWarp + kAttnWarps;
+constexpr int kQ8Threads = (kFirstDqWarp + 4) * 32;
 constexpr int kQ8TileBlocks = 8;                               // blocks per 128-token tile
 constexpr int kRawStageBytes = kQ8TileBlocks * kQ8TileBytes;   // 8 K (or V) tiles: 17408
 constexpr int kOpHalfBytes = 128 * 128;                        // 128 rows x 64 FP16 values
 constexpr int kOffKd = 0;                                      // K codes x 2, FP16 [128 tok][128 d]
-constexpr int kOffQbd = kOffKd + 2 * 2 * kOpHalfBytes;         // Qbd x 2, FP16 [16][128 d]
-constexpr int kOffP = kOffQbd + 2 * 4096;                      // P' per attention warp: [32 tok][16] FP32
+constexpr int kOffQbd = kOffKd + 2 * 2 * kOpHalfBytes;         // Qbd, FP16 [16][128 d]
+constexpr int kOffP = kOffQbd + 4096;                          // P' per attention warp: [32 tok][16] FP32
 constexpr int kOffMl = kOffP + kAttnWarps * 2048;              // unit merge: max, sum [8 warps][4 heads]
-constexpr int kOffRawK = kOffMl + 2 * kAttnWarps * 4 * 4;      // K ring
+constexpr int kScaleSlots = 4;                                 // K scales of a tile, for the softmax
+constexpr int kOffSk = kOffMl + 2 * kAttnWarps * 4 * 4;        // [slot][128 tokens][4] FP16
+constexpr int kOffRawK = kOffSk + kScaleSlots * 1024;          // K ring
 constexpr int kOffRawV = kOffRawK + kKStages * kRawStageBytes;  // V ring
 constexpr int kOffBarQ8 = kOffRawV + kVStages * kRawStageBytes;
-constexpr int kSmemQ8 = kOffBarQ8 + 256;
+constexpr int kSmemQ8 = kOffBarQ8 + 512;
 static_assert(kSmemQ8 <= 227 * 1024, "shared memory per CTA");
 static_assert(kOffRawK % 16 == 0 && kOffQbd % 1024 == 0 && kOffP % 16 == 0, "alignment");
 constexpr uint32_t kTmemColsQ8 = 32;  // S buffers at columns 0 and 16
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazyMax = 8.f;  // log2 units: weights stay below 2^8 (FP32 throughout)
 
 struct Q8Bars {
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t kd_full[2], kd_empty[2];
   uint64_t s_full[2], s_empty[2];
+  uint64_t sk_full[kScaleSlots];
   uint64_t merge[2];
   uint32_t tmem_base;
 };
-static_assert(sizeof(Q8Bars) <= 256, "barrier area");
+static_assert(sizeof(Q8Bars) <= 512, "barrier area");
 
 // One (request, KV head, split) of the launch.
 struct Unit {
@@ -197,21 +210,22 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      // 128 dequant threads, lane 0 of each attention warp, and the V producer
-      // (so no K stage is refilled before the V producer has seen it land)
-      mbar_init(&bars->k_empty[s], 128 + kAttnWarps + 1);
+      // 128 dequant threads and the V producer (so no K stage is refilled
+      // before the V producer has seen it land)
+      mbar_init(&bars->k_empty[s], 128 + 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], kAttnWarps);
+      mbar_init(&bars->v_empty[s], kAttnWarps / 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->kd_full[s], 128);
       mbar_init(&bars->kd_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_empty[s], kAttnWarps * 32);
+      mbar_init(&bars->s_empty[s], kAttnWarps / 2 * 32);
       mbar_init(&bars->merge[s], kAttnWarps);
     }
+    for (int s = 0; s < kScaleSlots; ++s) mbar_init(&bars->sk_full[s], 128);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -232,7 +246,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
     // about when the softmax needs it instead of occupying a stage for the
     // whole Q.K^T and softmax.  One copy per lane.  Block-table entries are
     // read 32 at a time (one per lane), one chunk ahead of use.
-    const bool is_v = warp == 1;
+    const bool is_v = warp >= kPerRing;
+    const int ppar = warp % kPerRing;  // this warp issues the tiles with i % kPerRing == ppar
     const int ns = is_v ? kVStages : kKStages;
     uint64_t* full = is_v ? bars->v_full : bars->k_full;
     uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
@@ -251,6 +266,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         if (slot == 0) nxt = entry(x.b0 + j * kQ8TileBlocks + 32 + lane);  // the next chunk, read ahead
         int blk = __shfl_sync(0xffffffffu, cur, slot * kQ8TileBlocks + (lane & (kQ8TileBlocks - 1)));
         if (slot == 3) cur = nxt;
+        if (i % kPerRing != ppar) continue;  // another warp's tile
         const int st = i % ns;
         const int nblk = min(kQ8TileBlocks, x.b1 - (x.b0 + j * kQ8TileBlocks));
         const bool copies = lane < nblk;
@@ -276,17 +292,18 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
     if (lane == 0) {
       if (!ok) report(a.err, PKV_DEVERR_TIMEOUT);
       // no copy may still be landing when the CTA's shared memory is released
-      for (int k = max(0, i - ns); k < i; ++k) mbar_wait(&full[k % ns], (k / ns) & 1);
+      for (int k = max(0, i - ns); k < i; ++k)
+        if (k % kPerRing == ppar) mbar_wait(&full[k % ns], (k / ns) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_f16_f32(128, 16, false, false);
-      int i = 0, uo = 0;  // tile index, non-empty unit ordinal (selects the Qbd buffer)
+      int i = 0;
+      const uint32_t qbd = sbase + kOffQbd;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
         const Unit x = unit_at(a, u);
         if (x.n_tiles == 0) continue;
-        const uint32_t qbd = sbase + kOffQbd + (uo & 1) * 4096;
         for (int j = 0; j < x.n_tiles; ++j, ++i) {
           const int b = i & 1;
           ok = mbar_wait(&bars->kd_full[b], (i >> 1) & 1);
@@ -304,7 +321,6 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
           tc::commit(&bars->s_full[b]);
           tc::commit(&bars->kd_empty[b]);
         }
-        ++uo;
       }
       if (!ok) report(a.err, PKV_DEVERR_TIMEOUT);
       // tensor memory is released only after the last MMA has finished
@@ -314,10 +330,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
   } else if (warp < kFirstDqWarp) {
     // ------------------------------ attention ------------------------------
     const int aw = warp - kFirstAttnWarp;  // 0..7
-    const int half = aw >> 2;          // this warp's tokens: 32w + 16*half .. +15 of every tile
+    const int par = aw >> 2;           // this warp's tiles: i % 2 == par (it reads S buffer par)
     const int w = warp & 3;            // TMEM sub-partition: tokens 32w .. 32w+31 of a tile
     const int k = w * 32 + lane;       // this thread's token row of S
-    const bool mine = (lane >> 4) == half;
     const int g_own = lane >> 3;       // group of this lane's dims 4*lane .. 4*lane+3
     const uint32_t lane_off = static_cast<uint32_t>(w * 32) << 16;
     uint8_t* pw = smem + kOffP + aw * 2048;  // this warp's P' (and, at a unit's end, its O)
@@ -351,8 +366,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         o[h][0] = o[h][1] = make_float2(0.f, 0.f);
       }
       for (int j = 0; j < x.n_tiles; ++j, ++i) {
-        const int sb = i & 1;
-        const int kst = i % kKStages;
+        if ((i & 1) != par) continue;  // the other group's tile
+        const int sb = par;
         const int vst = i % kVStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (i >> 1) & 1));
         if (!ok) break;
@@ -360,38 +375,43 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         float s[16];  // column 4g + h: group g's part of head h's dot product
         tc::tmem_ld16(tmem + lane_off + sb * 16, s);
         tc::tmem_wait_ld();
+        // this token's K scales, copied out of the K stage by the dequantisation;
+        // read before S is released, which orders the read before the slot's reuse
+        const int sks = i % kScaleSlots;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->sk_full[sks], (i / kScaleSlots) & 1));
+        if (!ok) break;
+        float sk[4], sv[4];
+        half4_to_float(*reinterpret_cast<const uint2*>(smem + kOffSk + sks * 1024 + k * 8), sk);
         tc::fence_before_sync();
         mbar_arrive(&bars->s_empty[sb]);
-        // K scales (the K stage landed before QK(i); waiting again orders this read after it)
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->k_full[kst], (i / kKStages) & 1));
-        if (!ok) break;
-        const uint8_t* rawk = smem + kOffRawK + kst * kRawStageBytes;
         const uint8_t* rawv = smem + kOffRawV + vst * kRawStageBytes;
         const int so = (k >> 4) * kQ8TileBytes + kQ8CodeBytes + (k & 15) * 8;
-        float sk[4], sv[4];
-        half4_to_float(*reinterpret_cast<const uint2*>(rawk + so), sk);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->k_empty[kst]);  // this warp is done with the K stage
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[vst], (i / kVStages) & 1));
         if (!ok) break;
         half4_to_float(*reinterpret_cast<const uint2*>(rawv + so), sv);
-        // the other warp of this sub-partition takes the other 16 tokens
-        const bool valid = mine && (x.b0 + j * kQ8TileBlocks) * kBlockSize + k < x.ctx_keys;
+        const bool valid = (x.b0 + j * kQ8TileBlocks) * kBlockSize + k < x.ctx_keys;
 #pragma unroll
         for (int q = 0; q < 4; ++q) sv[q] = valid ? sv[q] : 0.f;  // a slot past the data may hold any bits
-        float sc[4], alpha[4];
-        bool grew = false;
+        float sc[4], alpha[4] = {1.f, 1.f, 1.f, 1.f};
+        bool over = false;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const float dot = sk[0] * s[h] + sk[1] * s[4 + h] + sk[2] * s[8 + h] + sk[3] * s[12 + h];
           sc[h] = valid ? c0 * dot : -INFINITY;
-          float mt = sc[h];
+          over |= sc[h] > m[h] + kLazyMax || (m[h] == -INFINITY && valid);
+        }
+        const bool grew = __any_sync(0xffffffffu, over);  // warp-uniform
+        if (grew) {
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-          const float mn = fmaxf(m[h], mt);
-          alpha[h] = (mn == -INFINITY) ? 1.f : exp2_approx(m[h] - mn);  // 0 while m is -inf
-          grew |= mn != m[h];
-          m[h] = mn;
+          for (int h = 0; h < 4; ++h) {
+            float mt = sc[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            if (mt > m[h] + kLazyMax || (m[h] == -INFINITY && mt != -INFINITY)) {  // uniform: mt is the warp's
+              alpha[h] = exp2_approx(m[h] - mt);  // 0 while m is -inf
+              m[h] = mt;
+            }
+          }
         }
         // this token's weights P' = p * sV for the 4 groups x 4 heads
         float p[4];
@@ -413,12 +433,12 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
           }
         }
         __syncwarp();
-        // O += P' V over the warp's 16 tokens (block 2w + half): lane = dims 4*lane .. 4*lane+3
-        const uint8_t* vrow = rawv + (2 * w + half) * kQ8TileBytes + 4 * lane;
+        // O += P' V over the warp's 32 tokens: lane = dims 4*lane .. 4*lane+3
+        const uint8_t* vrow = rawv + (2 * w) * kQ8TileBytes + 4 * lane;
 #pragma unroll 8
-        for (int t = 0; t < 16; ++t) {
-          const uint32_t cw = *reinterpret_cast<const uint32_t*>(vrow + t * 128);
-          const float4 pv = *reinterpret_cast<const float4*>(pw + p_chunk(16 * half + t, g_own));
+        for (int t = 0; t < 32; ++t) {
+          const uint32_t cw = *reinterpret_cast<const uint32_t*>(vrow + (t >> 4) * kQ8TileBytes + (t & 15) * 128);
+          const float4 pv = *reinterpret_cast<const float4*>(pw + p_chunk(t, g_own));
           float2 c01, c23;
           codes_to_f32(cw, c01, c23);
           const float ph[4] = {pv.x, pv.y, pv.z, pv.w};
@@ -429,13 +449,13 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
             o[h][1] = __ffma2_rn(p2, c23, o[h][1]);
           }
         }
-        __syncwarp();  // P' is rewritten by the next tile
+        __syncwarp();  // P' is rewritten by the warp's next tile
         if (lane == 0) mbar_arrive(&bars->v_empty[vst]);
       }
       if (!ok) break;
 
-      // ---- unit epilogue: merge the 8 warps' (max, sum, O); a warp whose
-      // tokens were all past the data contributes max -inf and sum 0 ----
+      // ---- unit epilogue: merge the 8 warps' (max, sum, O); a warp without a
+      // tile (or a key) in this unit contributes max -inf and sum 0 ----
       float lw[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
@@ -483,14 +503,14 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
     }
     if (!ok && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
   } else {
-    // ------------------------------ K dequantisation (warps 11-14) ------------------------------
+    // ------------------------------ K dequantisation (last 4 warps) ------------------------------
     const int t128 = threadIdx.x - kFirstDqWarp * 32;
     const int cc = t128 & 15;  // 16-byte output chunk of a row: dims 8cc .. 8cc+7
     const int rsub = t128 >> 4;
     const int c = cc & 7;
     const int rbase = rsub * 128 + cc * 8;  // + (jj>>1)*2176 + (jj&1)*1024 for row jj*8 + rsub
     const int wbase = (cc >> 3) * kOpHalfBytes + rsub * 128 + ((c ^ rsub) << 4);  // + jj*1024
-    int i = 0, uo = 0;
+    int i = 0;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
       const Unit x = unit_at(a, u);
       if (x.n_tiles == 0) continue;
@@ -502,16 +522,22 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         const int b = i & 1;
         ok = mbar_wait(&bars->k_full[st], (i / kKStages) & 1);
         if (ok && i >= 2) ok = mbar_wait(&bars->kd_empty[b], ((i - 2) >> 1) & 1);  // QK(i-2) done
+        // the unit's first tile rewrites the query operand: the previous unit's last QK must be done
+        if (ok && j == 0 && i >= 1) ok = mbar_wait(&bars->kd_empty[(i - 1) & 1], ((i - 1) >> 1) & 1);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        const uint8_t* stage = smem + kOffRawK + st * kRawStageBytes;
+        // token t128's K scales for the softmax (slot i % 4 was last read by the
+        // softmax of tile i-4, which released S(i-4) before QK(i-2) ran)
+        *reinterpret_cast<uint2*>(smem + kOffSk + (i % kScaleSlots) * 1024 + t128 * 8) =
+            *reinterpret_cast<const uint2*>(stage + (t128 >> 4) * kQ8TileBytes + kQ8CodeBytes + (t128 & 15) * 8);
         if (j == 0) {
-          // the unit's block-diagonal query operand; the other buffer may still
-          // feed QK(i-1), this one was last read by a QK at or before i-2
+          // the unit's block-diagonal query operand
           const int d = t128;
           float qv[4];
 #pragma unroll
           for (int h = 0; h < 4; ++h) qv[h] = bf16_lo(qg[h * kHeadDim + d]) * qs;
-          uint8_t* qb = smem + kOffQbd + (uo & 1) * 4096 + (d >> 6) * 2048;
+          uint8_t* qb = smem + kOffQbd + (d >> 6) * 2048;
 #pragma unroll
           for (int n = 0; n < 16; ++n)
             *reinterpret_cast<__half*>(qb + tc::sw128_offset(n, d & 63)) =
@@ -519,7 +545,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         }
         // all 16 loads first: stores to the operand tile could alias them for
         // the compiler, which would otherwise serialise load -> store pairs
-        const uint8_t* raw = smem + kOffRawK + st * kRawStageBytes + rbase;
+        const uint8_t* raw = stage + rbase;
         uint8_t* dst = smem + kOffKd + b * 2 * kOpHalfBytes + wbase;
         uint2 wv[16];
 #pragma unroll
@@ -527,11 +553,11 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
           wv[jj] = *reinterpret_cast<const uint2*>(raw + (jj >> 1) * kQ8TileBytes + (jj & 1) * 1024);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) *reinterpret_cast<uint4*>(dst + jj * 1024) = codes_to_f16(wv[jj]);
-        tc::fence_proxy_async_smem();
+        tc::fence_proxy_async_smem();  // the operand tiles are read by the tensor core
         mbar_arrive(&bars->kd_full[b]);
+        mbar_arrive(&bars->sk_full[i % kScaleSlots]);
         mbar_arrive(&bars->k_empty[st]);
       }
-      ++uo;
     }
     if (!ok && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
   }
