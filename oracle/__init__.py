@@ -62,6 +62,14 @@ def _bind(lib):
     lib.oracle_paged_attention_f64.argtypes = [c_p, c_p, c_p, c_p, c_p, i32, i32, i32, i32, c_p, i32, c_p, i32, i32,
                                                i32, ctypes.c_double, i32]
     lib.oracle_paged_attention_f64.restype = ctypes.c_int
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_value.restype = ctypes.c_double
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_kv_append_fp8.argtypes = [c_p, c_p, i32, i32, i32, c_p, c_p, c_p, i32]
+    lib.oracle_kv_append_fp8.restype = None
+    lib.oracle_dequantize_fp8.argtypes = [c_p, c_p, ctypes.c_int64]
+    lib.oracle_dequantize_fp8.restype = None
     return lib
 
 
@@ -265,3 +273,37 @@ def paged_attention_f64(q, k_cache_f64, v_cache_f64, block_tables, context_lens,
     if rc != 0:
         raise ValueError("block table entry outside the pool")
     return (out, lse) if with_lse else out
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) KV (§8.4.4): uint8 pools [num_blocks][Hkv][16][128] of E4M3 codes.
+# ---------------------------------------------------------------------------
+FP8_TILE_BYTES = 2048
+
+
+def e4m3_value(code: int) -> float:
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def kv_append_fp8(k_cache: np.ndarray, v_cache: np.ndarray, slot_mapping, k_new, v_new, block_size: int = 16):
+    """In place: round new BF16 K/V rows to E4M3 and store them (pools uint8 [nb][Hkv][16][128])."""
+    assert k_cache.dtype == np.uint8 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    nb, hkv, bs, d = k_cache.shape
+    assert bs == block_size and d == 128
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    _load().oracle_kv_append_fp8(_ptr(k_cache), _ptr(v_cache), nb, block_size, hkv, _ptr(slot_mapping), _ptr(k_new),
+                                 _ptr(v_new), slot_mapping.shape[0])
+
+
+def dequantize_fp8(cache: np.ndarray) -> np.ndarray:
+    """E4M3 pool -> float64 pool of the same shape."""
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    out = np.zeros(cache.shape, np.float64)
+    _load().oracle_dequantize_fp8(_ptr(cache), _ptr(out), cache.size)
+    return out

@@ -307,3 +307,67 @@ int oracle_paged_attention_f64(double* out, double* out_lse, const uint16_t* q, 
   }
   return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * FP8 KV ("Chapter 8: Inference Optimization" §8.4.4: K and V stored in FP8,
+ * the query kept in BF16).  The pages do not fix the FP8 variant; this is the
+ * plain reading: OCP E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; subnormals below 2^-6; no infinities; magnitudes up to 448), each
+ * BF16 value rounded to the nearest E4M3 value, ties to even mantissa, finite
+ * values beyond 448 saturated to +-448, no scale.  Tile of one (block, kv
+ * head): E4M3 codes [16][128], 2048 bytes.
+ * --------------------------------------------------------------------------- */
+#define FP8_TILE_BYTES 2048
+
+/* Value of an E4M3 code (finite codes only; 0x7F / 0xFF are NaN). */
+double oracle_e4m3_value(uint8_t code) {
+  int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* Nearest E4M3 code of a finite value (round half to even, saturating). */
+uint8_t oracle_e4m3_encode(double x) {
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E; /* 448 = 1.75 * 2^8 */
+  /* magnitudes are ordered like their codes 0x00 .. 0x7E: bisect */
+  int lo = 0, hi = 0x7E;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (oracle_e4m3_value((uint8_t)mid) <= a) lo = mid;
+    else hi = mid;
+  }
+  double vlo = oracle_e4m3_value((uint8_t)lo), vhi = oracle_e4m3_value((uint8_t)hi);
+  int pick;
+  if (a - vlo < vhi - a) pick = lo;
+  else if (a - vlo > vhi - a) pick = hi;
+  else pick = (lo & 1) ? hi : lo; /* tie: the even code (even mantissa) */
+  if (a == vhi) pick = hi;
+  return sign | (uint8_t)pick;
+}
+
+/* Store each new token's K and V in its slot of E4M3 pools
+ * [num_blocks][num_kv_heads][16][128]; same slot rules as oracle_kv_append. */
+void oracle_kv_append_fp8(uint8_t* k_cache, uint8_t* v_cache, int32_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, const int64_t* slot_mapping, const uint16_t* k_new,
+                          const uint16_t* v_new, int32_t num_tokens) {
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= (int64_t)num_blocks * block_size) continue;
+    int64_t blk = slot / block_size;
+    int32_t off = (int32_t)(slot % block_size);
+    for (int32_t h = 0; h < num_kv_heads; ++h)
+      for (int32_t d = 0; d < 128; ++d) {
+        int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * 128 + d;
+        int64_t src = ((int64_t)t * num_kv_heads + h) * 128 + d;
+        k_cache[dst] = oracle_e4m3_encode(bf16_value(k_new[src]));
+        v_cache[dst] = oracle_e4m3_encode(bf16_value(v_new[src]));
+      }
+  }
+}
+
+/* E4M3 pool -> double pool of the same shape. */
+void oracle_dequantize_fp8(const uint8_t* cache, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(cache[i]);
+}

@@ -3,9 +3,9 @@
 Each mutant is a one-line edit of pkv_oracle.c of the kind a careless
 restatement might make (a dropped scale, an off-by-one causal rule, a wrong
 GQA group, a transposed cache index, a dropped normalisation, a wrong BF16
-decode, a wrong slot split, and the q8_0 quantiser's scale, rounding and
-layout).  The copy is compiled on the CPU and the pins of
-test_oracle_attention / test_oracle_sizes are run against it.
+decode, a wrong slot split, the q8_0 quantiser's scale, rounding and layout,
+and the FP8 encoder's rounding, bias, saturation and layout).  The copy is
+compiled on the CPU and the pins of the oracle tests are run against it.
 """
 import inspect
 
@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import test_oracle_attention as A
+import test_oracle_fp8 as F
 import test_oracle_q8 as Q
 import test_oracle_sizes as S
 
@@ -40,12 +41,20 @@ MUTANTS = {
     "q8_scale_group": ("(t * 4 + d / 32) * 2", "(t * 4 + d / 64) * 2"),
     "q8_groups_reversed": ("(int8_t*)(tile + off * 128 + 32 * g)", "(int8_t*)(tile + off * 128 + 32 * (3 - g))"),
     "q8_attention_reads_k_as_v": ("o[d] += w * v_cache[cache_index(", "o[d] += w * k_cache[cache_index("),
+    # FP8 E4M3 (§8.4.4): ties away from zero, wrong exponent bias, overflow to
+    # NaN instead of saturation, wrong subnormal step, transposed pool layout
+    "fp8_ties_away": ("else pick = (lo & 1) ? hi : lo;", "else pick = hi;"),
+    "fp8_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 6)"),
+    "fp8_no_saturation": ("if (a >= 448.0) return sign | 0x7E;", "if (a >= 448.0) return sign | 0x7F;"),
+    "fp8_subnormal_step": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    "fp8_layout": ("int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * 128 + d;",
+                   "int64_t dst = ((blk * block_size + off) * num_kv_heads + h) * 128 + d;"),
 }
 
 
 def _pins():
     fns = []
-    for mod in (A, Q, S):
+    for mod in (A, F, Q, S):
         for name, fn in inspect.getmembers(mod, inspect.isfunction):
             if name.startswith("test_") and fn.__module__ == mod.__name__:
                 fns.append((name, fn))
