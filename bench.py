@@ -67,13 +67,14 @@ WORKLOAD_TEXT = {
 }
 
 
-# q8_0 (§8.4.2): 34 bytes per 32 values instead of 64
+# q8_0 (§8.4.2): 34 bytes per 32 values instead of 64; FP8 (§8.4.4): one byte per value
 KV_BYTES_PER_TOKEN_Q8 = KV_BYTES_PER_TOKEN * 34 // 64
+KV_BYTES_PER_TOKEN_FP8 = KV_BYTES_PER_TOKEN // 2
 
 
 def bytes_per_layer(w, kv: str = "bf16"):
     """(attention algorithmic bytes, append bytes) of one layer-call."""
-    stored = KV_BYTES_PER_TOKEN_Q8 if kv == "q8_0" else KV_BYTES_PER_TOKEN
+    stored = {"q8_0": KV_BYTES_PER_TOKEN_Q8, "fp8_e4m3": KV_BYTES_PER_TOKEN_FP8}.get(kv, KV_BYTES_PER_TOKEN)
     uniq = w.unique_tokens()
     qo = 2 * w.num_seqs * w.q_len * w.num_q_heads * w.head_dim * 2
     table = sum(-(-int(c) // 16) for c in w.context_lens) * 4 + w.num_seqs * 4
@@ -201,7 +202,7 @@ def oracle_sample(w, kc_dev, vc_dev, max_seqs: int):
 
 
 def oracle_sample_q8(w, kq_dev, vq_dev, max_seqs: int):
-    """oracle_sample for q8_0 pools: host copies of the q8_0 tiles the sampled requests read."""
+    """oracle_sample for quantised pools: host copies of the tiles the sampled requests read."""
     seq_ids = list(range(min(max_seqs, w.num_seqs)))
     need = {}
     for r in seq_ids:
@@ -221,15 +222,16 @@ def oracle_sample_q8(w, kq_dev, vq_dev, max_seqs: int):
     return sub, kq, vq
 
 
-def time_oracle_q8(sub, kq, vq, budget_s: float = 12.0, max_reps: int = 200):
-    """The oracle's q8_0 append, dequantisation and FP64 attention on the sample."""
+def time_oracle_q8(sub, kq, vq, budget_s: float = 12.0, max_reps: int = 200, kv: str = "q8_0"):
+    """The oracle's quantising append, dequantisation and FP64 attention on the sample."""
     import oracle
-    attn_b, app_b = bytes_per_layer(sub, "q8_0")
+    attn_b, app_b = bytes_per_layer(sub, kv)
+    append = oracle.kv_append_q8_0 if kv == "q8_0" else oracle.kv_append_fp8
+    deq = oracle.dequantize_q8_0 if kv == "q8_0" else oracle.dequantize_fp8
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.kv_append_q8_0(kq, vq, sub.slot_mapping, sub.k_new, sub.v_new)
-        oracle.paged_attention_f64(sub.q, oracle.dequantize_q8_0(kq), oracle.dequantize_q8_0(vq), sub.block_tables,
-                                   sub.context_lens, 1, sub.scale)
+        append(kq, vq, sub.slot_mapping, sub.k_new, sub.v_new)
+        oracle.paged_attention_f64(sub.q, deq(kq), deq(vq), sub.block_tables, sub.context_lens, 1, sub.scale)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= max_reps:
@@ -275,8 +277,8 @@ def main():
     ap.add_argument("--suffix-blocks-per-split", type=int, default=0, help="cascade suffix pass split (0 = plan)")
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workloads: plain paged attention instead of the cascade call")
-    ap.add_argument("--kv", default="bf16", choices=["bf16", "q8_0"],
-                    help="KV pool format: bf16, or q8_0 (decode only; tensor-core dequantising kernel)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "q8_0", "fp8_e4m3"],
+                    help="KV pool format: bf16, q8_0 or fp8_e4m3 (the last two: decode only, dequantising kernel)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -296,9 +298,10 @@ def main():
     w, layers = make_workload(args.workload, args.seed, args.num_seqs)
     if args.layers > 0:
         layers = args.layers
-    q8 = args.kv == "q8_0"
+    q8 = args.kv in ("q8_0", "fp8_e4m3")  # a quantised pool (q8_0 or E4M3)
+    fp8 = args.kv == "fp8_e4m3"
     if q8 and w.q_len != 1:
-        raise SystemExit("--kv q8_0 is a decode (q_len 1) path")
+        raise SystemExit(f"--kv {args.kv} is a decode (q_len 1) path")
     attn_b, app_b = bytes_per_layer(w, args.kv)
     step_bytes = layers * (attn_b + app_b)
     tokens_layers = int(w.context_lens.sum()) * w.q_len * layers if w.q_len > 1 else int(w.context_lens.sum()) * layers
@@ -323,7 +326,8 @@ def main():
     # device state: per-layer pools (filled on the device), per-layer step inputs/outputs
     if q8:
         # BF16 values drawn on the device, quantised into each layer's q8_0 pool by the library's append
-        k_pool = torch.empty((layers, w.num_blocks, hkv, pkv.Q8_TILE_BYTES), dtype=torch.uint8, device=dev)
+        tile_shape = (16, d) if fp8 else (pkv.Q8_TILE_BYTES,)
+        k_pool = torch.empty((layers, w.num_blocks, hkv) + tile_shape, dtype=torch.uint8, device=dev)
         v_pool = torch.empty_like(k_pool)
         tmp_k = torch.empty((w.num_blocks, hkv, 16, d), dtype=torch.bfloat16, device=dev)
         tmp_v = torch.empty_like(tmp_k)
@@ -332,7 +336,8 @@ def main():
         for l in range(layers):
             W.fill_pool_device(tmp_k, 1000 + 2 * l + args.seed * 7919)
             W.fill_pool_device(tmp_v, 1001 + 2 * l + args.seed * 7919)
-            pkv.kv_append_q8_0(k_pool[l], v_pool[l], all_slots, tok(tmp_k), tok(tmp_v))
+            (pkv.kv_append_fp8_e4m3 if fp8 else pkv.kv_append_q8_0)(k_pool[l], v_pool[l], all_slots, tok(tmp_k),
+                                                                    tok(tmp_v))
         del tmp_k, tmp_v, all_slots
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -364,7 +369,7 @@ def main():
     stream = torch.cuda.Stream(dev)  # non-default: CUDA graphs can be captured on it
     torch.cuda.set_stream(stream)
     sp = stream.cuda_stream
-    pool_stride = w.num_blocks * hkv * (pkv.Q8_TILE_BYTES if q8 else 16 * d * 2)
+    pool_stride = w.num_blocks * hkv * (pkv.FP8_TILE_BYTES if fp8 else pkv.Q8_TILE_BYTES if q8 else 16 * d * 2)
     kp0, vp0 = k_pool.data_ptr(), v_pool.data_ptr()
     q_stride, kn_stride = b * ql * hq * d * 2, t_tok * hkv * d * 2
     launches_per_layer = 1 + 1 + (1 if (splits > 8 or (splits > 1 and (ql >= 16 or q8))) else 0)
@@ -388,16 +393,16 @@ def main():
             raise RuntimeError(f"{what}: {lib.pkv_status_string(st).decode()}")
 
     def layer_call(l, ev=None):
-        append = lib.pkv_kv_append_q8_0 if q8 else lib.pkv_kv_append
+        append = lib.pkv_kv_append_fp8_e4m3 if fp8 else lib.pkv_kv_append_q8_0 if q8 else lib.pkv_kv_append
         check(append(kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc), slots.data_ptr(),
                      kn.data_ptr() + l * kn_stride, vn.data_ptr() + l * kn_stride, t_tok, sp), "kv_append")
         if ev is not None:
             ev[0].record(stream)
         if q8:
-            check(lib.pkv_paged_attention_q8_0(out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride,
-                                               kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc),
-                                               tables.data_ptr(), maxb, ctx.data_ptr(), b, hq, w.scale, bps,
-                                               ws.data_ptr(), ws.numel(), sp), "paged_attention_q8_0")
+            attn = lib.pkv_paged_attention_fp8_e4m3 if fp8 else lib.pkv_paged_attention_q8_0
+            check(attn(out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride, kp0 + l * pool_stride,
+                       vp0 + l * pool_stride, ctypes.byref(desc), tables.data_ptr(), maxb, ctx.data_ptr(), b, hq,
+                       w.scale, bps, ws.data_ptr(), ws.numel(), sp), "paged_attention_" + args.kv)
         elif cascade:
             check(lib.pkv_paged_attention_cascade(
                 out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride, kp0 + l * pool_stride,
@@ -479,9 +484,10 @@ def main():
                 dst.copy_(src, non_blocking=True)
             for l in range(layers):
                 if q8:
-                    pkv.kv_append_q8_0(k_pool[l], v_pool[l], slots, kn[l], vn[l])
-                    pkv.paged_attention_q8_0(out[l], q[l], k_pool[l], v_pool[l], tables, ctx, w.scale,
-                                             kv_blocks_per_split=bps, workspace=ws)
+                    (pkv.kv_append_fp8_e4m3 if fp8 else pkv.kv_append_q8_0)(k_pool[l], v_pool[l], slots, kn[l], vn[l])
+                    (pkv.paged_attention_fp8_e4m3 if fp8 else pkv.paged_attention_q8_0)(
+                        out[l], q[l], k_pool[l], v_pool[l], tables, ctx, w.scale, kv_blocks_per_split=bps,
+                        workspace=ws)
                     continue
                 pkv.kv_append(k_pool[l], v_pool[l], slots, kn[l], vn[l])
                 if cascade:
@@ -509,7 +515,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         if q8:
             sub, kq_h, vq_h = oracle_sample_q8(w, k_pool[0], v_pool[0], max_seqs=w.num_seqs)
-            r = time_oracle_q8(sub, kq_h, vq_h, budget_s=args.oracle_budget_s)
+            r = time_oracle_q8(sub, kq_h, vq_h, budget_s=args.oracle_budget_s, kv=args.kv)
         else:
             sub = oracle_sample(w, k_pool[0], v_pool[0], max_seqs=w.num_seqs)
             r = time_oracle(sub, budget_s=args.oracle_budget_s)
@@ -532,13 +538,14 @@ def main():
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
-        tj = json.load(open(tpath)).get(args.workload + ("_q8_0" if q8 else ""))
+        tj = json.load(open(tpath)).get(args.workload + ("_" + args.kv if q8 else ""))
         if tj and tj.get("kernel_build") == kernel_build_id():
             traffic = tj.get("bytes_per_launch")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "q8_0 KV, f16 tensor-core products, f32 softmax" if q8 else "bf16",
+        "vs_baseline": None,
+        "dtype": f"{args.kv} KV, f16 tensor-core Q.K, f32 softmax and P.V" if q8 else "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_seqs": b, "q_len": ql,
                    "layers": layers, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16,
@@ -557,8 +564,8 @@ def main():
         "bytes_per_step": int(step_bytes),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
-                     "kernel": ("paged_attention_q8_0 call (tensor-core q8_0 decode%s)" % (
-                                    " + combine" if splits > 1 else "") if q8 else
+                     "kernel": ("paged_attention_%s call (tensor-core dequantising decode%s)" % (
+                                    args.kv, " + combine" if splits > 1 else "") if q8 else
                                 "paged_attention_cascade call (prefix tensor-core pass + suffix decode + combine)"
                                 if cascade else "paged_attention call (%s%s)" % (
                                     "tensor-core chunk" if ql >= 16 else "decode",

@@ -354,14 +354,14 @@ pkv_status pkv_kv_append_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc
 
 /*
  * pkv_choose_kv_blocks_per_split_q8_0 -- blocks per split for
- * pkv_paged_attention_q8_0: its kernel keeps one persistent CTA per SM, so
+ * pkv_paged_attention_q8_0 and pkv_paged_attention_fp8_e4m3: their kernel keeps one persistent CTA per SM, so
  * the split count is the one that best balances (request, KV head, split)
  * units over sm_count CTAs (0 = current device), in whole 8-block tiles.
  */
 int32_t pkv_choose_kv_blocks_per_split_q8_0(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
                                             int32_t sm_count);
 
-/* Workspace bytes pkv_paged_attention_q8_0 needs (0 when there is one split). */
+/* Workspace bytes pkv_paged_attention_q8_0 (and the FP8 call) needs (0 when there is one split). */
 size_t pkv_workspace_size_q8_0(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                int32_t kv_blocks_per_split);
 
@@ -385,6 +385,43 @@ pkv_status pkv_paged_attention_q8_0(void* out, const void* q, const void* k_cach
 pkv_status pkv_copy_blocks_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
                                 const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
                                 void* stream);
+
+/*
+ * ---------------------------------------------------------------------------
+ * FP8 KV cache (§8.4.4 "Capacity and speed under a quality constraint": K and
+ * V stored in FP8 while the query stays BF16).  The page does not fix the FP8
+ * variant; this library uses OCP E4M3 (4 exponent bits, bias 7, 3 mantissa
+ * bits, subnormals, no infinities, |x| <= 448), rounding each BF16 value to
+ * the nearest E4M3 value (ties to even) and saturating finite values beyond
+ * 448 to +-448; there is no scale.  Inputs must be finite.
+ *
+ * Pool layout, per tensor: uint8 [num_blocks][num_kv_heads][16][128] E4M3
+ * codes (PKV_FP8_TILE_BYTES per (block, kv head)); `cache` as for BF16 pools.
+ * ---------------------------------------------------------------------------
+ */
+#define PKV_FP8_TILE_BYTES 2048u
+
+/* pkv_kv_append_fp8_e4m3 -- pkv_kv_append for E4M3 pools (rounding as above). */
+pkv_status pkv_kv_append_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                  const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                                  int32_t num_tokens, void* stream);
+
+/*
+ * pkv_paged_attention_fp8_e4m3 -- one decode step over E4M3 pools with the
+ * query in BF16: out = softmax(scale * q . K^T) V on the stored values.
+ * Arguments, split choice (pkv_choose_kv_blocks_per_split_q8_0), workspace
+ * (pkv_workspace_size_q8_0) and errors exactly as pkv_paged_attention_q8_0.
+ */
+pkv_status pkv_paged_attention_fp8_e4m3(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                        const pkv_cache_desc* cache, const int32_t* block_tables,
+                                        int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, float scale, int32_t kv_blocks_per_split,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* pkv_copy_blocks for E4M3 pools (num_kv_heads * PKV_FP8_TILE_BYTES per block). */
+pkv_status pkv_copy_blocks_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                    const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                                    void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* pkv_status_string(pkv_status status);

@@ -24,7 +24,8 @@ __all__ = [
     "cascade_workspace_size", "attn_combine", "workspace_size",
     "choose_kv_blocks_per_split", "get_device_error", "library_path", "lib", "DEVERR_BLOCK_ID",
     "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "Q8_TILE_BYTES", "kv_append_q8_0", "paged_attention_q8_0",
-    "choose_kv_blocks_per_split_q8_0", "workspace_size_q8_0", "copy_blocks_q8_0",
+    "choose_kv_blocks_per_split_q8_0", "workspace_size_q8_0", "copy_blocks_q8_0", "FP8_TILE_BYTES",
+    "kv_append_fp8_e4m3", "paged_attention_fp8_e4m3", "copy_blocks_fp8_e4m3",
 ]
 
 DEVERR_BLOCK_ID = 1
@@ -100,6 +101,13 @@ def _load():
     lib.pkv_paged_attention_q8_0.restype = ctypes.c_int
     lib.pkv_copy_blocks_q8_0.argtypes = [p, p, ctypes.POINTER(CacheDesc), p, p, i32, p]
     lib.pkv_copy_blocks_q8_0.restype = ctypes.c_int
+    lib.pkv_kv_append_fp8_e4m3.argtypes = [p, p, ctypes.POINTER(CacheDesc), p, p, p, i32, p]
+    lib.pkv_kv_append_fp8_e4m3.restype = ctypes.c_int
+    lib.pkv_paged_attention_fp8_e4m3.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32, f32, i32,
+                                                 p, sz, p]
+    lib.pkv_paged_attention_fp8_e4m3.restype = ctypes.c_int
+    lib.pkv_copy_blocks_fp8_e4m3.argtypes = [p, p, ctypes.POINTER(CacheDesc), p, p, i32, p]
+    lib.pkv_copy_blocks_fp8_e4m3.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.pkv_get_device_error.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -430,6 +438,80 @@ def copy_blocks_q8_0(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: t
     _check(_lib.pkv_copy_blocks_q8_0(k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
                                      src_blocks.data_ptr(), dst_blocks.data_ptr(), src_blocks.numel(),
                                      _stream_ptr(stream)), "pkv_copy_blocks_q8_0")
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) KV pools: uint8 [num_blocks][num_kv_heads][16][128] codes.
+# ---------------------------------------------------------------------------
+FP8_TILE_BYTES = 2048
+
+
+def _fp8_pool(t: torch.Tensor, name: str) -> CacheDesc:
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA uint8 (or float8_e4m3fn) tensor")
+    if t.dim() != 4 or t.shape[2] != BLOCK_SIZE or t.shape[3] != HEAD_DIM:
+        raise ValueError(f"{name} must be [num_blocks][num_kv_heads][16][128]")
+    return CacheDesc(t.shape[0], BLOCK_SIZE, t.shape[1], HEAD_DIM)
+
+
+def kv_append_fp8_e4m3(k_cache: torch.Tensor, v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                       k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    """Round k_new/v_new [T][Hkv][128] (BF16) to E4M3 and store them at slot_mapping[T]."""
+    desc = _fp8_pool(k_cache, "k_cache")
+    _fp8_pool(v_cache, "v_cache")
+    _bf16(k_new, "k_new"), _bf16(v_new, "v_new")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous CUDA int64 tensor")
+    t = slot_mapping.numel()
+    if tuple(k_new.shape) != (t, desc.num_kv_heads, HEAD_DIM) or tuple(v_new.shape) != k_new.shape:
+        raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][128]")
+    _check(_lib.pkv_kv_append_fp8_e4m3(k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+                                       slot_mapping.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), t,
+                                       _stream_ptr(stream)), "pkv_kv_append_fp8_e4m3")
+
+
+def paged_attention_fp8_e4m3(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                             kv_blocks_per_split: int = 0, workspace: torch.Tensor | None = None,
+                             stream=None) -> None:
+    """Decode step (q_len 1) over E4M3 pools with a BF16 query: out[B][1][Hq][128]."""
+    desc = _fp8_pool(k_cache, "k_cache")
+    _fp8_pool(v_cache, "v_cache")
+    _bf16(out, "out"), _bf16(q, "q")
+    _i32(block_tables, "block_tables"), _i32(context_lens, "context_lens")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
+    b = context_lens.numel()
+    if q.dim() != 4 or q.shape[0] != b or q.shape[1] != 1 or out.shape != q.shape:
+        raise ValueError("q/out must be [num_seqs][1][num_q_heads][128]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != b:
+        raise ValueError("block_tables must be [num_seqs][max_blocks_per_seq]")
+    maxb = block_tables.shape[1]
+    bps = kv_blocks_per_split or choose_kv_blocks_per_split_q8_0(b, desc.num_kv_heads, maxb)
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(_lib.pkv_paged_attention_fp8_e4m3(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                             ctypes.byref(desc), block_tables.data_ptr(), maxb,
+                                             context_lens.data_ptr(), b, q.shape[2], float(scale), bps, ws_ptr,
+                                             ws_bytes, _stream_ptr(stream)), "pkv_paged_attention_fp8_e4m3")
+
+
+def copy_blocks_fp8_e4m3(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: torch.Tensor,
+                         dst_blocks: torch.Tensor, stream=None) -> None:
+    """copy_blocks for E4M3 pools."""
+    desc = _fp8_pool(k_cache, "k_cache")
+    _fp8_pool(v_cache, "v_cache")
+    _i32(src_blocks, "src_blocks"), _i32(dst_blocks, "dst_blocks")
+    if src_blocks.numel() != dst_blocks.numel():
+        raise ValueError("src_blocks and dst_blocks differ in length")
+    _check(_lib.pkv_copy_blocks_fp8_e4m3(k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+                                         src_blocks.data_ptr(), dst_blocks.data_ptr(), src_blocks.numel(),
+                                         _stream_ptr(stream)), "pkv_copy_blocks_fp8_e4m3")
 
 
 def get_device_error(reset: bool = True) -> int:

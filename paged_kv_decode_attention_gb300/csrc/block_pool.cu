@@ -194,6 +194,29 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
              : PKV_ERR_CUDA;
 }
 
+static pkv_status copy_blocks_bytes(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                    const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                                    int32_t tile_bytes, void* stream) {
+  if (cache == nullptr) return PKV_ERR_NULL;
+  if (cache->num_blocks < 0 || cache->num_kv_heads <= 0 || num_pairs < 0) return PKV_ERR_SHAPE;
+  if (cache->block_size != kBlockSize || cache->head_dim != kHeadDim) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_blocks || !dst_blocks) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs > (1 << 30)) return PKV_ERR_UNSUPPORTED;
+  return launch_copy_blocks(k_cache, v_cache, cache->num_blocks, static_cast<int64_t>(cache->num_kv_heads) * tile_bytes,
+                            src_blocks, dst_blocks, num_pairs, device_error_word(),
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                    const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                                    void* stream) {
+  return copy_blocks_bytes(k_cache, v_cache, cache, src_blocks, dst_blocks, num_pairs, kFp8TileBytes, stream);
+}
+
 pkv_status pkv_copy_blocks_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
                                 const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
                                 void* stream) {

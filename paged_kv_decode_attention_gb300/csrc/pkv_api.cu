@@ -399,11 +399,17 @@ size_t pkv_workspace_size_q8_0(int32_t num_seqs, int32_t num_q_heads, int32_t ma
   return align_up(rows * splits * kHeadDim * sizeof(float), 256) + align_up(rows * splits * sizeof(float), 256);
 }
 
-pkv_status pkv_paged_attention_q8_0(void* out, const void* q, const void* k_cache, const void* v_cache,
-                                    const pkv_cache_desc* cache, const int32_t* block_tables,
-                                    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
-                                    int32_t num_q_heads, float scale, int32_t kv_blocks_per_split, void* workspace,
-                                    size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Decode over quantised pools (q8_0, or E4M3 when fp8): validation, split
+// choice, workspace carving, the decode kernel and the combine pass.
+pkv_status quantised_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
+                               int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes, void* stream,
+                               bool fp8) {
   pkv_status st = check_cache(cache);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_blocks_per_seq < 1 || kv_blocks_per_split < 0) return PKV_ERR_SHAPE;
@@ -442,7 +448,7 @@ pkv_status pkv_paged_attention_q8_0(void* out, const void* q, const void* k_cach
   const int sms = device_sm_count();
   const int32_t grid = static_cast<int32_t>(units < sms ? units : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (splits == 1) return launch_paged_decode_q8(a, grid, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  if (splits == 1) return launch_paged_decode_q8(a, grid, fp8, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
   const size_t need = pkv_workspace_size_q8_0(num_seqs, num_q_heads, max_blocks_per_seq, bps);
   if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
@@ -450,9 +456,50 @@ pkv_status pkv_paged_attention_q8_0(void* out, const void* q, const void* k_cach
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                         align_up(rows * splits * kHeadDim * sizeof(float), 256));
-  if (launch_paged_decode_q8(a, grid, s) != cudaSuccess) return PKV_ERR_CUDA;
+  if (launch_paged_decode_q8(a, grid, fp8, s) != cudaSuccess) return PKV_ERR_CUDA;
   return launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), splits, s) ==
                  cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_q8_0(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                    const pkv_cache_desc* cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                    int32_t num_q_heads, float scale, int32_t kv_blocks_per_split, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  return quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                             num_seqs, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream,
+                             false);
+}
+
+pkv_status pkv_paged_attention_fp8_e4m3(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                        const pkv_cache_desc* cache, const int32_t* block_tables,
+                                        int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, float scale, int32_t kv_blocks_per_split,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  return quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                             num_seqs, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream,
+                             true);
+}
+
+pkv_status pkv_kv_append_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                  const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                                  int32_t num_tokens, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !slot_mapping || !k_new || !v_new) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return PKV_ERR_UNSUPPORTED;
+  return launch_kv_append_fp8(k_cache, v_cache, cache->num_blocks, cache->num_kv_heads, slot_mapping, k_new, v_new,
+                              num_tokens, error_word(), static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
 }

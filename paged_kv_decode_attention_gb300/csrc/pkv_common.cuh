@@ -22,6 +22,8 @@ constexpr int kTileBytes = kBlockSize * kHeadDim * 2;  // one (block, kv head) t
 // scale of every 32-value group, [16][4]: 64 groups of 34 bytes.
 constexpr int kQ8CodeBytes = kBlockSize * kHeadDim;                  // 2048
 constexpr int kQ8TileBytes = kQ8CodeBytes + kBlockSize * kHeadDim / 32 * 2;  // 2176
+// FP8 (E4M3) tile of one (block, kv head): codes [16][128], no scale.
+constexpr int kFp8TileBytes = kBlockSize * kHeadDim;  // 2048
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s: a healthy wait takes microseconds
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

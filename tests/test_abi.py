@@ -156,3 +156,27 @@ def test_q8_argument_errors():
     assert call(b=0) == 0
     assert lib.pkv_copy_blocks_q8_0(p, p, ctypes.byref(_desc(block_size=8)), p, p, 1, None) == 3
     assert lib.pkv_copy_blocks_q8_0(p, p, d, p, p, 0, None) == 0
+
+
+def test_fp8_argument_errors():
+    lib = pkv.lib()
+    p = ctypes.c_void_p(256)
+    d = ctypes.byref(_desc())
+    assert lib.pkv_kv_append_fp8_e4m3(p, p, None, p, p, p, 1, None) == 1
+    assert lib.pkv_kv_append_fp8_e4m3(p, p, ctypes.byref(_desc(block_size=8)), p, p, p, 1, None) == 3
+    assert lib.pkv_kv_append_fp8_e4m3(p, p, d, p, p, p, -2, None) == 2
+    assert lib.pkv_kv_append_fp8_e4m3(p, p, d, p, p, p, 0, None) == 0
+
+    def call(**kw):
+        a = dict(out=p, q=p, k=p, v=p, desc=d, bt=p, maxb=64, cl=p, b=2, hq=32, scale=0.1, bps=16, ws=None, wsb=0)
+        a.update(kw)
+        return lib.pkv_paged_attention_fp8_e4m3(a["out"], a["q"], a["k"], a["v"], a["desc"], a["bt"], a["maxb"],
+                                                a["cl"], a["b"], a["hq"], a["scale"], a["bps"], a["ws"], a["wsb"],
+                                                None)
+
+    assert call(desc=None) == 1
+    assert call(hq=16) == 3
+    assert call(scale=float("nan")) == 2
+    assert call() == 4
+    assert call(b=0) == 0
+    assert lib.pkv_copy_blocks_fp8_e4m3(p, p, d, p, p, 0, None) == 0
