@@ -62,7 +62,7 @@ namespace {
 // Pipeline depth (8 KiB per stage) and the CTAs per SM the register budget
 // targets; compile-time knobs so the depth can be swept.
 #ifndef PKV_DECODE_STAGES
-#define PKV_DECODE_STAGES 8
+#define PKV_DECODE_STAGES 12
 #endif
 #ifndef PKV_DECODE_MIN_CTAS
 #define PKV_DECODE_MIN_CTAS 2

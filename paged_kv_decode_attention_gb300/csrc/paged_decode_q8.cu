@@ -467,25 +467,34 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
           }
         }
         __syncwarp();
-        // O += P' V over the warp's 32 tokens: lane = dims 4*lane .. 4*lane+3
+        // O += P' V over the warp's 32 tokens: lane = dims 4*lane .. 4*lane+3.
+        // Only keys that hold data: in a ragged last tile the other slots may
+        // hold any bits, and an E4M3 NaN pattern times a zero weight is NaN.
+        const int nkeys = x.ctx_keys - (x.b0 + j * kQ8TileBlocks) * kBlockSize - 32 * w;
         const uint8_t* vrow = rawv + (2 * w) * kQ8TileBytes + 4 * lane;
+        auto pv_keys = [&](int n) {
 #pragma unroll 8
-        for (int t = 0; t < 32; ++t) {
-          const uint32_t cw = *reinterpret_cast<const uint32_t*>(vrow + (t >> 4) * kQ8TileBytes + (t & 15) * 128);
-          const float4 pv = *reinterpret_cast<const float4*>(pw + p_chunk(t, g_own));
-          float2 c01, c23;
-          if constexpr (kQ8)
-            codes_to_f32(cw, c01, c23);
-          else
-            e4m3x4_to_f32(cw, c01, c23);
-          const float ph[4] = {pv.x, pv.y, pv.z, pv.w};
+          for (int t = 0; t < n; ++t) {
+            const uint32_t cw = *reinterpret_cast<const uint32_t*>(vrow + (t >> 4) * kQ8TileBytes + (t & 15) * 128);
+            const float4 pv = *reinterpret_cast<const float4*>(pw + p_chunk(t, g_own));
+            float2 c01, c23;
+            if constexpr (kQ8)
+              codes_to_f32(cw, c01, c23);
+            else
+              e4m3x4_to_f32(cw, c01, c23);
+            const float ph[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float2 p2 = make_float2(ph[h], ph[h]);
-            o[h][0] = __ffma2_rn(p2, c01, o[h][0]);
-            o[h][1] = __ffma2_rn(p2, c23, o[h][1]);
+            for (int h = 0; h < 4; ++h) {
+              const float2 p2 = make_float2(ph[h], ph[h]);
+              o[h][0] = __ffma2_rn(p2, c01, o[h][0]);
+              o[h][1] = __ffma2_rn(p2, c23, o[h][1]);
+            }
           }
-        }
+        };
+        if (nkeys >= 32)
+          pv_keys(32);  // every tile but a unit's last: a fixed trip count
+        else
+          pv_keys(nkeys);
         __syncwarp();  // P' is rewritten by the warp's next tile
         if (lane == 0) mbar_arrive(&bars->v_empty[vst]);
       }

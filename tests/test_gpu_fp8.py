@@ -148,6 +148,29 @@ def test_fp8_ragged_contexts_and_splits(bps):
     assert_close(bf16_to_f64(out), oracle_fp8(q, kq, vq, tables, ctx, scale), what=f"fp8 ragged bps={bps}")
 
 
+def unused_slots(tables, ctx, nb):
+    """(block, offset) pairs no context covers."""
+    used = np.zeros((nb, 16), bool)
+    for r, c in enumerate(ctx):
+        for t in range(int(c)):
+            used[tables[r, t // 16], t % 16] = True
+    return np.argwhere(~used)
+
+
+@pytest.mark.parametrize("bps", [0, 5])
+def test_fp8_nan_patterns_in_unused_slots(bps):
+    """Slots past every context hold E4M3 NaN codes (0x7F, 0xFF): a zero
+    weight times NaN is NaN, so those keys must not enter P.V at all."""
+    q, kq, vq, tables, ctx = _ragged(12, [1, 17, 129, 250, 333])
+    kq, vq = kq.copy(), vq.copy()
+    for n, (blk, off) in enumerate(unused_slots(tables, ctx, kq.shape[0])):
+        kq[blk, :, off] = 0x7F if n % 2 else 0xFF
+        vq[blk, :, off] = 0xFF if n % 2 else 0x7F
+    scale = 128 ** -0.5
+    out = run_fp8(dev(q), dev(kq), dev(vq), dev(tables), dev(ctx), scale, bps=bps)
+    assert_close(bf16_to_f64(out), oracle_fp8(q, kq, vq, tables, ctx, scale), what=f"fp8 NaN slots bps={bps}")
+
+
 def test_fp8_empty_context_and_many_units():
     rng = np.random.default_rng(7)
     ctx = rng.integers(0, 400, size=48)

@@ -183,6 +183,31 @@ def test_q8_many_units_per_cta():
     assert_close(bf16_to_f64(out), oracle_q8(q, kq, vq, tables, ctx, scale), what="q8 many units")
 
 
+def unused_slots(tables, ctx, nb):
+    """(block, offset) pairs no context covers: the tails of last blocks and
+    blocks no table reaches within its context."""
+    used = np.zeros((nb, 16), bool)
+    for r, c in enumerate(ctx):
+        for t in range(int(c)):
+            used[tables[r, t // 16], t % 16] = True
+    return np.argwhere(~used)
+
+
+@pytest.mark.parametrize("bps", [0, 5])
+def test_q8_nan_patterns_in_unused_slots(bps):
+    """Slots past every context hold NaN scales and extreme codes: they must
+    never reach a result (ragged last tiles read them into shared memory)."""
+    q, kq, vq, tables, ctx = _ragged(12, [1, 17, 129, 250, 333])
+    kq, vq = kq.copy(), vq.copy()
+    for blk, off in unused_slots(tables, ctx, kq.shape[0]):
+        for pool in (kq, vq):
+            pool[blk, :, off * 128:(off + 1) * 128] = 0x7F
+            pool[blk, :, 2048 + off * 8:2048 + (off + 1) * 8] = 0xFF  # FP16 NaN scales
+    scale = 128 ** -0.5
+    out = run_q8(dev(q), dev(kq), dev(vq), dev(tables), dev(ctx), scale, bps=bps)
+    assert_close(bf16_to_f64(out), oracle_q8(q, kq, vq, tables, ctx, scale), what=f"q8 NaN slots bps={bps}")
+
+
 def test_q8_large_queries_are_rescaled_into_fp16_range():
     """Queries of magnitude ~2^20 (beyond FP16) with the scale shrunk to
     match: the kernel shifts them by a power of two, the result is unchanged."""
