@@ -428,6 +428,23 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
 // host side: tensor maps over a KV pool viewed as rows of 128 BF16
 // ---------------------------------------------------------------------------
 
+template <bool kSplit>
+cudaError_t allow_smem_tc() {
+  static bool done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(paged_chunk_tc_kernel<kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -457,23 +474,6 @@ bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-template <bool kSplit>
-cudaError_t allow_smem_tc() {
-  static bool done[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!done[dev]) {
-    e = cudaFuncSetAttribute(paged_chunk_tc_kernel<kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
-    if (e != cudaSuccess) return e;
-    done[dev] = true;
-  }
-  return cudaSuccess;
-}
-
-}  // namespace
 
 cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, int32_t grid_x, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;

@@ -224,15 +224,23 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
       const uint8_t* vbase = static_cast<const uint8_t*>(a.v_cache);
       bool ok = true;
       int issued = 0;
-      for (int base = 0; base < n_iter && ok; base += 32) {
-        int blk = 0;
+      // block ids of a 32-block chunk, one per lane, validated (a bad id
+      // reads block 0); -1 past the range
+      auto chunk = [&](int base) -> int {
+        int b = -1;
         if (base + lane < n_iter) {
-          blk = table[base + lane];
-          if (blk < 0 || blk >= a.num_blocks) {
+          b = table[base + lane];
+          if (b < 0 || b >= a.num_blocks) {
             report(a.err, PKV_DEVERR_BLOCK_ID);
-            blk = 0;
+            b = 0;
           }
         }
+        return b;
+      };
+      int blk_next = chunk(0);
+      for (int base = 0; base < n_iter && ok; base += 32) {
+        const int blk = blk_next;
+        blk_next = chunk(base + 32);  // the next chunk's ids, read while this one streams
         const int cnt = min(32, n_iter - base);
         for (int u = 0; u < cnt; ++u) {
           const int pb = __shfl_sync(kFull, blk, u);

@@ -42,12 +42,15 @@ namespace {
 
 unsigned int* error_word() { return device_error_word(); }
 
+// SM count assumed when no device can be queried (host-only sizing): GB300.
+constexpr int kGb300Sms = 152;
+
 int device_sm_count() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kGb300Sms;
   if (g_sm_count[dev] == 0) {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kGb300Sms;
     g_sm_count[dev] = n;
   }
   return g_sm_count[dev];
@@ -69,6 +72,41 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr int kMinBlocksPerSplit = 16;
 constexpr int kResidentCtasPerSm = 2;
 constexpr int kTcMinBlocksPerSplit = 128;
+
+// Decode batches with at least this many (request, KV head) rows per SM run
+// on the persistent tensor-core kernel: with two CTAs per SM already busy,
+// one CTA streaming 192 KiB of tiles per SM wastes less on per-CTA fill and
+// drain (measured: 64 x 32K tokens 0.98 vs 0.88 of the HBM peak, 512 x 512
+// 0.89 vs 0.80); smaller batches keep the CTA-per-row kernel.
+constexpr int kTcDecodeRowsPerSm = 2;
+
+bool decode_on_tensor_cores(int64_t num_seqs, int64_t num_kv_heads, int32_t q_len, int sm_count) {
+  return q_len == 1 && num_seqs * num_kv_heads >= static_cast<int64_t>(kTcDecodeRowsPerSm) * sm_count;
+}
+
+// Split size for the persistent kernels (one CTA per SM walking units of
+// 8-block tiles): minimise the makespan -- the busiest CTA runs
+// ceil(units / SMs) units, each costing its tiles plus about one tile of
+// pipeline fill and epilogue -- with 2 tiles charged for the combine pass.
+int32_t persistent_blocks_per_split(int64_t rows, int32_t max_blocks_per_seq, int32_t sm_count) {
+  int32_t best = max_blocks_per_seq;
+  int64_t best_cost = INT64_MAX;
+  for (int32_t splits = 1; splits <= 64; ++splits) {
+    int32_t bps = (max_blocks_per_seq + splits - 1) / splits;
+    bps = (bps + 7) / 8 * 8;
+    if (splits > 1 && bps < 16) break;
+    if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
+    const int64_t s_eff = (max_blocks_per_seq + bps - 1) / bps;
+    const int64_t units = rows * s_eff;
+    const int64_t per_cta = (units + sm_count - 1) / sm_count;
+    const int64_t cost = per_cta * ((bps + 7) / 8 + 1) + (s_eff > 1 ? 2 : 0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bps;
+    }
+  }
+  return best;
+}
 
 }  // namespace
 }  // namespace pkv
@@ -118,6 +156,8 @@ int32_t pkv_choose_kv_blocks_per_split(int32_t num_seqs, int32_t num_kv_heads, i
   }
   if (sm_count <= 0) sm_count = device_sm_count();
   const int64_t rows = static_cast<int64_t>(num_seqs) * (q_len > 0 ? q_len : 1) * num_kv_heads;
+  if (decode_on_tensor_cores(num_seqs, num_kv_heads, q_len, sm_count))
+    return persistent_blocks_per_split(rows, max_blocks_per_seq, sm_count);
   const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
   if (rows <= 0 || max_blocks_per_seq <= kMinBlocksPerSplit) return max_blocks_per_seq;
   // as many splits as fit in one wave: a few CTAs spilling into a second wave
@@ -136,7 +176,8 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, 
       kv_blocks_per_split <= 0 || kv_blocks_per_split >= max_blocks_per_seq)
     return 0;
   const size_t splits = (static_cast<size_t>(max_blocks_per_seq) + kv_blocks_per_split - 1) / kv_blocks_per_split;
-  if (q_len < kTcMinQLen && splits <= static_cast<size_t>(kMaxClusterSplits))
+  if (q_len < kTcMinQLen && splits <= static_cast<size_t>(kMaxClusterSplits) &&
+      !decode_on_tensor_cores(num_seqs, num_q_heads / kGroup, q_len, device_sm_count()))
     return 0;  // decode splits merge inside a thread-block cluster
   const size_t rows = static_cast<size_t>(num_seqs) * q_len * num_q_heads;
   return align_up(rows * splits * head_dim * sizeof(float), 256) + align_up(rows * splits * sizeof(float), 256);
@@ -187,6 +228,25 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
   const int32_t tc_grid_x = num_seqs * ((q_len + 15) / 16);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = device_sm_count();
+  if (decode_on_tensor_cores(num_seqs, cache->num_kv_heads, q_len, sms)) {
+    const int64_t units = static_cast<int64_t>(num_seqs) * cache->num_kv_heads * splits;
+    if (units > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    const int32_t grid = static_cast<int32_t>(units < sms ? units : sms);
+    if (splits == 1) return launch_paged_decode_tc(a, grid, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const size_t need = pkv_workspace_size(num_seqs, 1, num_q_heads, kHeadDim, max_blocks_per_seq, bps);
+    if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                          align_up(rows * splits * kHeadDim * sizeof(float), 256));
+    if (launch_paged_decode_tc(a, grid, s) != cudaSuccess) return PKV_ERR_CUDA;
+    return launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), splits, s) ==
+                   cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+  }
   const bool tensor_cores = q_len >= kTcMinQLen;
   if (splits > kMaxClusterSplits || (tensor_cores && splits > 1)) {
     const size_t need = pkv_workspace_size(num_seqs, q_len, num_q_heads, kHeadDim, max_blocks_per_seq, bps);
@@ -367,26 +427,7 @@ int32_t pkv_choose_kv_blocks_per_split_q8_0(int32_t num_seqs, int32_t num_kv_hea
   if (max_blocks_per_seq <= 0) return 1;
   if (sm_count <= 0) sm_count = device_sm_count();
   const int64_t rows = static_cast<int64_t>(num_seqs > 0 ? num_seqs : 1) * (num_kv_heads > 0 ? num_kv_heads : 1);
-  // Makespan of the persistent grid in 8-block tiles: the busiest CTA runs
-  // ceil(units / SMs) units; each unit costs its tiles plus about one tile of
-  // pipeline fill and epilogue, and splitting adds the combine pass.
-  int32_t best = max_blocks_per_seq;
-  int64_t best_cost = INT64_MAX;
-  for (int32_t splits = 1; splits <= 64; ++splits) {
-    int32_t bps = (max_blocks_per_seq + splits - 1) / splits;
-    bps = (bps + 7) / 8 * 8;
-    if (splits > 1 && bps < 16) break;
-    if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
-    const int64_t s_eff = (max_blocks_per_seq + bps - 1) / bps;
-    const int64_t units = rows * s_eff;
-    const int64_t per_cta = (units + sm_count - 1) / sm_count;
-    const int64_t cost = per_cta * ((bps + 7) / 8 + 1) + (s_eff > 1 ? 2 : 0);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = bps;
-    }
-  }
-  return best;
+  return persistent_blocks_per_split(rows, max_blocks_per_seq, sm_count);
 }
 
 size_t pkv_workspace_size_q8_0(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <utility>
 
@@ -110,6 +111,15 @@ constexpr int kTcMinQLen = 16;
 // shared prefix blocks, read through the first member's table row.
 using ChunkArgs = DecodeArgs;
 cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, int32_t grid_x, cudaStream_t stream);
+
+// Tensor map over a BF16 KV pool viewed as `rows` rows of 128 elements, boxes
+// of 16 rows x 64 elements with the 128-byte swizzle (paged_chunk_tc.cu).
+bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows);
+
+// Decode (q_len 1) with QK^T and PV on tensor cores, `grid` persistent CTAs
+// striding over the (request, KV head, split) units; num_splits > 1 writes
+// workspace partials for the combine kernel (paged_decode_tc.cu).
+cudaError_t launch_paged_decode_tc(const DecodeArgs& a, int32_t grid, cudaStream_t stream);
 
 // Members per cascade group: 16 requests x 4 heads = one 64-row tile.
 constexpr int kCascadeGroup = 16;
