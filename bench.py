@@ -372,7 +372,11 @@ def main():
     pool_stride = w.num_blocks * hkv * (pkv.FP8_TILE_BYTES if fp8 else pkv.Q8_TILE_BYTES if q8 else 16 * d * 2)
     kp0, vp0 = k_pool.data_ptr(), v_pool.data_ptr()
     q_stride, kn_stride = b * ql * hq * d * 2, t_tok * hkv * d * 2
-    launches_per_layer = 1 + 1 + (1 if (splits > 8 or (splits > 1 and (ql >= 16 or q8))) else 0)
+    # append + attention (+ the combine pass when splits go through the workspace: more than 8
+    # splits, or any split on the tensor-core paths -- chunks, quantised pools and q_len-1 batches
+    # of at least 2 (request, KV head) rows per SM)
+    tc_decode = ql == 1 and b * hkv >= 2 * torch.cuda.get_device_properties(dev).multi_processor_count
+    launches_per_layer = 1 + 1 + (1 if (splits > 8 or (splits > 1 and (ql >= 16 or q8 or tc_decode))) else 0)
     # shared prefixes: the caller states the groups and the cascade call reads each prefix once per group
     gs_h, gb_h, sp_h = W.prefix_groups(w)
     cascade = (not args.no_cascade) and gs_h.shape[0] > 0 and ql == 1 and not q8
