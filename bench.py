@@ -587,13 +587,17 @@ def main():
 def run_sweep(args):
     """q_len-1 stress sweep: batch x context grid, one layer, default split;
     L2 flushed (a 256 MiB write) before every timed call so small points are
-    read from HBM too.  Prints one JSON line with every point."""
+    read from HBM too, then a 256 MiB read evicts the flush's dirty lines so
+    their write-back is not charged to the call, and a device-side delay
+    covers the host's launch of the call so the events time the device work.
+    Prints one JSON line with every point."""
     import paged_kv_decode_attention_gb300 as pkv
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    drain = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB read after the flush
     free, _ = torch.cuda.mem_get_info(dev)
     batches = [int(x) for x in args.sweep_batches.split(",")] if args.sweep_batches else W.SWEEP_BATCHES
     contexts = [int(x) for x in args.sweep_contexts.split(",")] if args.sweep_contexts else W.SWEEP_CONTEXTS
@@ -622,6 +626,8 @@ def run_sweep(args):
             times = []
             for it in range(args.warmup + args.sweep_reps):
                 flush.fill_(it & 0xFF)
+                drain.sum()
+                torch.cuda._sleep(200000)  # ~100 us: the call below is enqueued before the GPU reaches it
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 pkv.paged_attention(out, q, kc, vc, tables, ctx, 1, w.scale, kv_blocks_per_split=bps, workspace=ws)
