@@ -97,7 +97,11 @@ cudaError_t launch_attn_combine(void* out, float* out_lse, const float* part_o, 
                                 int32_t num_rows, int32_t num_splits, cudaStream_t stream) {
   if (num_rows == 0) return cudaSuccess;
   uint16_t* o = static_cast<uint16_t*>(out);
-  if (num_splits >= 8)
+  // four warps per row only when the rows are too few to fill the GPU: with
+  // many rows, one warp per row keeps more rows' loads in flight
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (num_splits >= 8 && num_rows < 16 * sms)
     return launch_pdl(attn_combine_kernel<4>, dim3(static_cast<unsigned>(num_rows)), dim3(kThreadsCombine), 0,
                       stream, 1, o, out_lse, part_o, part_lse, num_rows, num_splits);
   return launch_pdl(attn_combine_kernel<1>, dim3(static_cast<unsigned>((num_rows + 3) / 4)), dim3(kThreadsCombine), 0,
