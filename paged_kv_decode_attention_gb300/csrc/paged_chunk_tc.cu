@@ -13,21 +13,26 @@
 //
 // CTA = 6 warps, one (request, row tile, split, KV head); 2 CTAs per SM:
 //   warp 0  : TMA producer.  A KV tile is 4 blocks (64 tokens): for each block
-//             two 16x64 boxes of K and two of V (128-byte swizzle) land in a
-//             3-stage ring; blocks past the range are fetched at an
-//             out-of-range row so TMA fills them with zeros.
+//             two 16x64 boxes of K and two of V (128-byte swizzle), issued by
+//             16 lanes at once, land in the KV ring; blocks past the range are
+//             fetched at an out-of-range row so TMA fills them with zeros.
 //   warp 1  : MMA issuer (one thread).  S_j = Q K_j^T (M 64, N 64, 8 k-steps,
 //             Q and K from shared memory) into a double-buffered TMEM S;
-//             O += P_j V_j (M 64, N 128, 4 k-steps, P from TMEM, V from shared
-//             memory) into TMEM O.  S_{j+1} is issued before waiting for P_j
-//             so QK^T overlaps the softmax.
+//             O += P_j V_j (M 64, N 128, 2 x 4 k-steps, P from TMEM, V from
+//             shared memory) into TMEM O.  The thread polls both and issues
+//             whichever is ready, so QK^T of the next tile overlaps the
+//             softmax and neither waits behind the other.
 //   warps 2-5: softmax.  Thread = one row (TMEM lanes 0-15 of each 32-lane
 //             sub-partition hold an M=64 accumulator).  Scores are masked
 //             (causal and context), scaled into base 2, exponentiated against
 //             a lazily updated row max (O in TMEM is rescaled only when a row
-//             max grows by more than 2^8), and written back as BF16 P over the
-//             S buffer they came from, the A operand of the next PV MMA.
+//             max grows by more than 2^8), and written back over the S buffer
+//             they came from as the A operands of the next PV MMAs: the BF16
+//             weights, then the BF16 roundings of their remainders (so P.V
+//             carries the weights to about 2^-17 relative, as an FP32 P
+//             would within the output's BF16 rounding).
 //   epilogue: O / l to BF16 (one split) or FP32 + lse (split-KV partials).
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -39,14 +44,7 @@
 namespace pkv {
 namespace {
 
-// KV ring depth (32 KiB per stage): with P kept in tensor memory, 16 KiB of
-// Q plus 3 stages fit twice into an SM's shared memory.
-#ifndef PKV_TC_STAGES
-#define PKV_TC_STAGES 3
-#endif
 constexpr int kTcThreads = 192;
-constexpr int kTcStages = PKV_TC_STAGES;
-constexpr int kTcMinCtas = kTcStages <= 3 ? 2 : 1;
 constexpr int kTileBlocks = 4;                        // KV blocks per tile
 constexpr int kTileTokens = kTileBlocks * kBlockSize;  // 64
 constexpr int kRows = 64;                             // 16 positions x 4 heads
@@ -55,21 +53,28 @@ constexpr int kHalfBytes = kTileTokens * 128;         // 64 tokens x 64 dims = 8
 constexpr int kStageBytesTc = 4 * kHalfBytes;         // K lo/hi, V lo/hi: 32 KiB
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
+// KV ring depth (32 KiB per stage): with P kept in tensor memory, 16 KiB of
+// Q plus 3 stages fit twice into an SM's shared memory (2 CTAs per SM, 96 KiB
+// of K/V in flight each).
+constexpr int kTcStages = 3;
 constexpr int kOffBar = kOffKV + kTcStages * kStageBytesTc;
 constexpr int kSmemTc = kOffBar + 256;
-constexpr uint32_t kTmemCols = 256;  // S/P buffer 0 [0,64), buffer 1 [64,128), O [128,256)
-constexpr uint32_t kColO = 128;
+static_assert(kSmemTc <= 113 * 1024, "two CTAs per SM");
+// Tensor memory: two S/P buffers of 64 columns (S_j in FP32; then P_j over
+// it, its BF16 high parts in the first 32 columns and the BF16 remainders in
+// the next 32), then O (128 columns).
+constexpr int kNB = 2;
+constexpr uint32_t kColO = kNB * 64;
+constexpr uint32_t kTmemCols = 256;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: weights stay below 2^8
 constexpr float kLn2 = 0.6931471805599453f;
-
-static_assert(kSmemTc <= (kTcMinCtas == 2 ? 113 : 227) * 1024, "shared memory per CTA");
 
 struct TcBars {
   uint64_t kv_full[kTcStages];
   uint64_t kv_empty[kTcStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_done[2];
+  uint64_t s_full[kNB];
+  uint64_t p_full[kNB];
+  uint64_t o_done[kNB];
   uint32_t tmem_base;
 };
 static_assert(sizeof(TcBars) <= 256, "barrier area");
@@ -150,7 +155,7 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kNB; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 128);
       mbar_init(&bars->o_done[s], 1);
@@ -167,19 +172,28 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
   }
   if (warp >= 2) {
     // Q rows (position, head) -> 128-byte swizzled K-major tile, two 64-dim halves
+    // thread t loads 16-byte chunk t % 16 of rows t / 16 + 8k, k < 8: all
+    // loads issued before the first store, so the (member, query) load chain
+    // costs two round trips, not eight
     const int t = threadIdx.x - 64;  // 0..127
+    const int ch = t & 15;           // 16-byte chunk of the row
     const uint16_t* qbase = static_cast<const uint16_t*>(a.q);
-    for (int idx = t; idx < kRows * 16; idx += 128) {
-      const int m = idx >> 4;
-      const int ch = idx & 15;  // 16-byte chunk of the row
+    constexpr int kPerThread = kRows * 16 / 128;
+    uint4 v[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int m = (t >> 4) + 8 * k;
       const int ipm = row_pos(m);
       const int rm = row_req(m);
-      uint4 v = make_uint4(0, 0, 0, 0);
+      v[k] = make_uint4(0, 0, 0, 0);
       if (rm >= 0 && ipm < a.q_len)
-        v = *reinterpret_cast<const uint4*>(
+        v[k] = *reinterpret_cast<const uint4*>(
             qbase + ((static_cast<int64_t>(rm) * a.q_len + ipm) * hq + kvh * kGroup + (m & 3)) * kHeadDim + ch * 8);
-      const int half = ch >> 3;
-      *reinterpret_cast<uint4*>(smem + kOffQ + half * 8192 + tc::sw128_offset(m, (ch & 7) * 8)) = v;
+    }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int m = (t >> 4) + 8 * k;
+      *reinterpret_cast<uint4*>(smem + kOffQ + (ch >> 3) * 8192 + tc::sw128_offset(m, (ch & 7) * 8)) = v[k];
     }
     tc::fence_proxy_async_smem();
   }
@@ -196,38 +210,38 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
     const int32_t* table = a.block_tables + static_cast<int64_t>(table_row) * a.max_blocks;
     const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;  // first row past the pool
     const int n_blocks = b1 - b0;
-    for (int base = 0; base < n_tiles * kTileBlocks && ok; base += 32) {
-      int y = oob_row;
-      if (base + lane < n_blocks) {
-        int blk = table[b0 + base + lane];
-        if (blk < 0 || blk >= a.num_blocks) {
-          report(a.err, PKV_DEVERR_BLOCK_ID);
-          blk = 0;
-        }
-        y = (blk * a.num_kv_heads + kvh) * kBlockSize;
+    // block id of block base + lane of the range, INT_MIN past it
+    auto chunk = [&](int base) -> int { return base + lane < n_blocks ? table[b0 + base + lane] : INT_MIN; };
+    // its pool row (a bad id reads block 0); past the range, the first row
+    // past the pool (zero fill)
+    auto row_of = [&](int blk) -> int {
+      if (blk == INT_MIN) return oob_row;
+      if (blk < 0 || blk >= a.num_blocks) {
+        report(a.err, PKV_DEVERR_BLOCK_ID);
+        blk = 0;
       }
-      const int cnt = min(32, n_tiles * kTileBlocks - base);
-      for (int u = 0; u < cnt; ++u) {
-        const int yy = __shfl_sync(0xffffffffu, y, u);
-        const int bi = base + u;
-        const int j = bi / kTileBlocks;
-        const int b = bi % kTileBlocks;
-        const int st = j % kTcStages;
-        if (lane == 0) {
-          if (b == 0) {
-            if (j >= kTcStages) ok = mbar_wait(&bars->kv_empty[st], ((j / kTcStages) & 1) ^ 1);
-            if (ok) mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytesTc);
-          }
-          if (ok) {
-            uint8_t* stg = smem + kOffKV + st * kStageBytesTc;
-            tc::tma_load_2d(stg + 0 * kHalfBytes + b * 2048, &k_map, 0, yy, &bars->kv_full[st], policy);
-            tc::tma_load_2d(stg + 1 * kHalfBytes + b * 2048, &k_map, 64, yy, &bars->kv_full[st], policy);
-            tc::tma_load_2d(stg + 2 * kHalfBytes + b * 2048, &v_map, 0, yy, &bars->kv_full[st], policy);
-            tc::tma_load_2d(stg + 3 * kHalfBytes + b * 2048, &v_map, 64, yy, &bars->kv_full[st], policy);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+      return (blk * a.num_kv_heads + kvh) * kBlockSize;
+    };
+    // Block ids are read 32 at a time (8 tiles), one chunk ahead, and checked
+    // only when their chunk is used, so the next chunk's load stays in flight.
+    // The 16 boxes of a tile (4 blocks x K/V x two 64-dim halves) are issued
+    // by 16 lanes at once: lane 4b + c takes block b, piece c (K lo, K hi,
+    // V lo, V hi).
+    int cur = row_of(chunk(0)), nxt = INT_MIN;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int slot = j & 7;
+      if (slot == 0) nxt = chunk((j + 8) * kTileBlocks);
+      const int yy = __shfl_sync(0xffffffffu, cur, slot * kTileBlocks + ((lane >> 2) & 3));
+      if (slot == 7) cur = row_of(nxt);
+      const int st = j % kTcStages;
+      if (j >= kTcStages) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((j / kTcStages) & 1) ^ 1));
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytesTc);
+      __syncwarp();
+      if (lane < 4 * kTileBlocks) {
+        const int b = lane >> 2, c = lane & 3;
+        tc::tma_load_2d(smem + kOffKV + st * kStageBytesTc + c * kHalfBytes + b * 2048, c < 2 ? &k_map : &v_map,
+                        (c & 1) * 64, yy, &bars->kv_full[st], policy);
       }
     }
     if (lane == 0) {
@@ -241,39 +255,57 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16_f32(kRows, kTileTokens, false, false);
       constexpr uint32_t kIdO = tc::idesc_bf16_f32(kRows, kHeadDim, false, true);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kTcStages;
-        const int sb = j & 1;
-        if (!mbar_wait(&bars->kv_full[st], (j / kTcStages) & 1)) return false;
-        // buffer sb holds P_{j-2} until PV_{j-2} has consumed it
-        if (j >= 2 && !mbar_wait(&bars->o_done[sb], ((j - 2) >> 1) & 1)) return false;
-        tc::fence_after_sync();
-        const uint32_t kst = sbase + kOffKV + st * kStageBytesTc;
+      // Two cursors: S_js needs its K tile and its buffer back (the P.V that
+      // last read it done), P.V_jp needs P_jp.  The thread polls both and
+      // issues whichever is ready, so neither waits behind the other.
+      int js = 0, jp = 0;
+      uint64_t t_idle = 0;
+      while (jp < n_tiles) {
+        bool progressed = false;
+        if (js < n_tiles) {
+          const int st = js % kTcStages, sb = js % kNB;
+          bool ready = mbar_test_wait(&bars->kv_full[st], (js / kTcStages) & 1);
+          if (ready && js >= kNB) ready = mbar_test_wait(&bars->o_done[sb], ((js / kNB) - 1) & 1);
+          if (ready) {
+            tc::fence_after_sync();
+            const uint32_t kst = sbase + kOffKV + st * kStageBytesTc;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t qa = sbase + kOffQ + (kk >> 2) * 8192 + 32 * (kk & 3);
-          const uint32_t ka = kst + (kk >> 2) * kHalfBytes + 32 * (kk & 3);
-          tc::mma_bf16(tmem + sb * 64, tc::smem_desc(qa, 16, 1024), tc::smem_desc(ka, 16, 1024), kIdS, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t qa = sbase + kOffQ + (kk >> 2) * 8192 + 32 * (kk & 3);
+              const uint32_t ka = kst + (kk >> 2) * kHalfBytes + 32 * (kk & 3);
+              tc::mma_bf16(tmem + sb * 64, tc::smem_desc(qa, 16, 1024), tc::smem_desc(ka, 16, 1024), kIdS, kk > 0);
+            }
+            tc::commit(&bars->s_full[sb]);
+            ++js;
+            progressed = true;
+          }
         }
-        tc::commit(&bars->s_full[sb]);
-        return true;
-      };
-      ok = issue_s(0);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles) ok = issue_s(j + 1);
-        if (ok) ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const int st = j % kTcStages;
-        const uint32_t ptm = tmem + (j & 1) * 64;  // P_j: 64 BF16 per row packed in 32 columns
-        const uint32_t vst = sbase + kOffKV + st * kStageBytesTc + 2 * kHalfBytes;
+        if (jp < js && mbar_test_wait(&bars->p_full[jp % kNB], (jp / kNB) & 1)) {
+          tc::fence_after_sync();
+          const int st = jp % kTcStages;
+          // P_jp: 64 BF16 high parts per row packed in 32 columns, then the remainders
+          const uint32_t ptm = tmem + (jp % kNB) * 64;
+          const uint32_t vst = sbase + kOffKV + st * kStageBytesTc + 2 * kHalfBytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_bf16_tmem_a(tmem + kColO, ptm + 8 * kk, tc::smem_desc(vst + 2048 * kk, kHalfBytes, 1024), kIdO,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_bf16_tmem_a(tmem + kColO, ptm + 32 * part + 8 * kk,
+                                  tc::smem_desc(vst + 2048 * kk, kHalfBytes, 1024), kIdO,
+                                  (jp > 0 || part > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(&bars->o_done[jp % kNB]);
+          tc::commit(&bars->kv_empty[st]);
+          ++jp;
+          progressed = true;
         }
-        tc::commit(&bars->o_done[j & 1]);
-        tc::commit(&bars->kv_empty[st]);
+        if (progressed) {
+          t_idle = 0;
+        } else if (t_idle == 0) {
+          t_idle = global_timer_ns();
+        } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) report(a.err, PKV_DEVERR_TIMEOUT);
     }
@@ -292,10 +324,10 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
     float m_stale = -INFINITY;     // scaled max the weights are taken against (lags the true max by < 2^8)
     float l = 0.f;                 // this thread's half of the row's weight sum
     for (int j = 0; j < n_tiles && ok; ++j) {
-      const int sb = j & 1;
+      const int sb = j % kNB;
       const int st = j % kTcStages;
       // keep `ok` warp-uniform: the tcgen05 loads below are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j >> 1) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j / kNB) & 1));
       if (!ok) break;
       tc::fence_after_sync();
       float s[32];  // raw scores of tokens half*32 .. half*32+31 of the tile
@@ -319,7 +351,7 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       const float alpha = grow ? exp2_approx(m_stale - m_new) : 1.f;  // 0 while m_stale is -inf
       if (__any_sync(0xffffffffu, grow && j > 0 && m_stale != -INFINITY)) {
         // O holds weights taken against the old maxima: rescale this warp's rows
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[(j - 1) % kNB], ((j - 1) / kNB) & 1));
         tc::fence_after_sync();
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -337,8 +369,10 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       const float nm = (m_stale == -INFINITY) ? 0.f : -m_stale;
       const float2 c2 = make_float2(c, c);
       const float2 nm2 = make_float2(nm, nm);
-      // P_j overwrites the S_j buffer it came from: 2 BF16 per 32-bit column
-      uint32_t pk[16];
+      // P_j overwrites the S_j buffer it came from, 2 BF16 per 32-bit column:
+      // the weights' BF16 roundings, then the BF16 roundings of what they
+      // left out, so P.V carries the weights to about 2^-17 relative
+      uint32_t pk[16], pr[16];
       float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -347,8 +381,10 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
         const float p1 = exp2_approx(x.y);
         acc2 = __fadd2_rn(acc2, make_float2(p0, p1));
         pk[e] = pack_bf16x2(p0, p1);
+        pr[e] = pack_bf16x2(p0 - __uint_as_float(pk[e] << 16), p1 - __uint_as_float(pk[e] & 0xffff0000u));
       }
       tc::tmem_st16x2_16<16>(tmem + lane_off + sb * 64, pk);
+      tc::tmem_st16x2_16<16>(tmem + lane_off + sb * 64 + 32, pr);
       l += acc2.x + acc2.y;
       // slots past the request's data in its last block may hold anything: zero those V rows
       const int tile0 = (b0 + j * kTileBlocks) * kBlockSize;
@@ -371,7 +407,7 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
     }
     if (!ok && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
     // ---- epilogue: this thread writes dims half*64 .. half*64+63 of its row ----
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[(n_tiles - 1) % kNB], ((n_tiles - 1) / kNB) & 1));
     tc::fence_after_sync();
     const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
     const float inv = (l_row > 0.f) ? 1.f / l_row : 0.f;
@@ -416,7 +452,7 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
 }
 
 template <bool kSplit>
-__global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
+__global__ void __launch_bounds__(kTcThreads, 2)
     paged_chunk_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                           const ChunkArgs a) {
   pdl_wait();  // inputs come from earlier grids in the stream
@@ -429,7 +465,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinCtas)
 // ---------------------------------------------------------------------------
 
 template <bool kSplit>
-cudaError_t allow_smem_tc() {
+cudaError_t launch_chunk_variant(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkArgs& a, dim3 grid,
+                                 cudaStream_t stream) {
   static bool done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -440,7 +477,7 @@ cudaError_t allow_smem_tc() {
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
-  return cudaSuccess;
+  return launch_pdl(paged_chunk_tc_kernel<kSplit>, grid, dim3(kTcThreads), kSmemTc, stream, 1, kmap, vmap, a);
 }
 
 }  // namespace
@@ -483,13 +520,9 @@ cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, int32_t grid_x, cudaStream
   const dim3 grid(static_cast<unsigned>(grid_x), static_cast<unsigned>(a.num_splits),
                   static_cast<unsigned>(a.num_kv_heads));
   if (grid.x == 0) return cudaSuccess;
-  cudaError_t e;
-  if (a.part_o != nullptr) {  // partials to the workspace (splits, or a cascade prefix pass)
-    if ((e = allow_smem_tc<true>()) != cudaSuccess) return e;
-    return launch_pdl(paged_chunk_tc_kernel<true>, grid, dim3(kTcThreads), kSmemTc, stream, 1, kmap, vmap, a);
-  }
-  if ((e = allow_smem_tc<false>()) != cudaSuccess) return e;
-  return launch_pdl(paged_chunk_tc_kernel<false>, grid, dim3(kTcThreads), kSmemTc, stream, 1, kmap, vmap, a);
+  // partials to the workspace (splits, or a cascade prefix pass), or BF16 out
+  return a.part_o != nullptr ? launch_chunk_variant<true>(kmap, vmap, a, grid, stream)
+                             : launch_chunk_variant<false>(kmap, vmap, a, grid, stream);
 }
 
 }  // namespace pkv

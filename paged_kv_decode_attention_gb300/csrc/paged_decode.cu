@@ -51,6 +51,7 @@
 //              second kernel;
 //   kWorkspace more splits: each writes its normalised FP32 output and
 //              natural-log lse to the workspace for the combine kernel.
+#include <climits>
 #include <cmath>
 
 #include "pkv_common.cuh"
@@ -107,29 +108,43 @@ constexpr float kLog2eF = 1.4426950408889634f;
 // Fold the cascade prefix pass's partials of one output row into a running
 // (max in base-2 logits, weight sum, un-normalised dims d0..d0+3).  A partial
 // (normalised O_s, natural-log lse_s) is a block of total weight 1 at the
-// base-2 logit lse_s * log2 e.
+// base-2 logit lse_s * log2 e.  The slots are read 8 at a time with every
+// load issued before the first is used.
 __device__ __forceinline__ void fold_prefix(const DecodeArgs& a, int64_t orow, int d0, float& mx, float& sum,
                                             float* o) {
-  const float* lse = a.prefix_lse + orow * a.prefix_slots;
-  float m2 = mx;
-  for (int sl = 0; sl < a.prefix_slots; ++sl) m2 = fmaxf(m2, lse[sl] * kLog2eF);
-  if (m2 == -INFINITY) return;
-  const float sc_old = exp2_approx(mx - m2);  // 0 when nothing was accumulated yet
-  sum *= sc_old;
+  constexpr int kChunk = 8;
+  const int ns = a.prefix_slots;
+  const float* lse = a.prefix_lse + orow * ns;
+  const float* po = a.prefix_o + orow * ns * kHeadDim + d0;
+  for (int s0 = 0; s0 < ns; s0 += kChunk) {
+    float ls[kChunk];
+    float4 v[kChunk];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) o[e] *= sc_old;
-  for (int sl = 0; sl < a.prefix_slots; ++sl) {
-    const float ls = lse[sl];
-    if (ls == -INFINITY) continue;
-    const float w = exp2_approx(ls * kLog2eF - m2);
-    sum += w;
-    const float4 v = *reinterpret_cast<const float4*>(a.prefix_o + (orow * a.prefix_slots + sl) * kHeadDim + d0);
-    o[0] = fmaf(w, v.x, o[0]);
-    o[1] = fmaf(w, v.y, o[1]);
-    o[2] = fmaf(w, v.z, o[2]);
-    o[3] = fmaf(w, v.w, o[3]);
+    for (int k = 0; k < kChunk; ++k) {
+      const int sl = s0 + k;
+      ls[k] = sl < ns ? lse[sl] * kLog2eF : -INFINITY;
+      v[k] = sl < ns ? *reinterpret_cast<const float4*>(po + sl * kHeadDim) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m2 = mx;
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) m2 = fmaxf(m2, ls[k]);
+    if (m2 == -INFINITY) continue;
+    const float sc_old = exp2_approx(mx - m2);  // 0 when nothing was accumulated yet
+    sum *= sc_old;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] *= sc_old;
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      if (ls[k] == -INFINITY) continue;  // an empty prefix split: its output is never used
+      const float w = exp2_approx(ls[k] - m2);
+      sum += w;
+      o[0] = fmaf(w, v[k].x, o[0]);
+      o[1] = fmaf(w, v[k].y, o[1]);
+      o[2] = fmaf(w, v[k].z, o[2]);
+      o[3] = fmaf(w, v[k].w, o[3]);
+    }
+    mx = m2;
   }
-  mx = m2;
 }
 
 template <int NS, SplitMode kMode>
@@ -224,22 +239,20 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
       const uint8_t* vbase = static_cast<const uint8_t*>(a.v_cache);
       bool ok = true;
       int issued = 0;
-      // block ids of a 32-block chunk, one per lane, validated (a bad id
-      // reads block 0); -1 past the range
-      auto chunk = [&](int base) -> int {
-        int b = -1;
-        if (base + lane < n_iter) {
-          b = table[base + lane];
-          if (b < 0 || b >= a.num_blocks) {
-            report(a.err, PKV_DEVERR_BLOCK_ID);
-            b = 0;
-          }
+      // block ids of a 32-block chunk, one per lane (INT_MIN past the range);
+      // validated only when the chunk is used (a bad id reads block 0), so the
+      // load of the next chunk stays in flight while this one streams
+      auto chunk = [&](int base) -> int { return base + lane < n_iter ? table[base + lane] : INT_MIN; };
+      auto checked = [&](int b) -> int {
+        if (b != INT_MIN && (b < 0 || b >= a.num_blocks)) {
+          report(a.err, PKV_DEVERR_BLOCK_ID);
+          b = 0;
         }
         return b;
       };
       int blk_next = chunk(0);
       for (int base = 0; base < n_iter && ok; base += 32) {
-        const int blk = blk_next;
+        const int blk = checked(blk_next);
         blk_next = chunk(base + 32);  // the next chunk's ids, read while this one streams
         const int cnt = min(32, n_iter - base);
         for (int u = 0; u < cnt; ++u) {

@@ -96,3 +96,67 @@ def test_cascade_full_size_workloads(name):
     gs, gb, sp = W.prefix_groups(w)
     out = run_cascade(w, gs, gb, sp)
     assert_close(bf16_to_f64(out), oracle.run_workload(w), what=f"cascade {name}")
+
+
+def large_cascade_batch(seed, prefix_blocks=12):
+    """A batch of 24+ requests: 21 sharers of a prefix (two groups), the rest
+    outside every group, one padding row (context 0) and one member whose
+    context ends inside the prefix."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = max(24, -(-sms // 16) + 6)
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(prefix_blocks * 16 + 1, prefix_blocks * 16 + 600, size=n)
+    ctx[n - 1] = 0
+    ctx[n - 2] = 37
+    sharers = [i < 21 for i in range(n)]
+    need = prefix_blocks + int(sum(-(-int(c) // 16) for c in ctx))
+    w = _shared(ctx, prefix_blocks, sharers, need + 32, seed=seed)
+    gs, gb, sp = W.prefix_groups(w)
+    assert gs.shape[0] == 2
+    w.context_lens[3] = prefix_blocks * 16 - 40  # a member ending inside its prefix
+    return w, gs, gb, sp
+
+
+def nan_unused(w):
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.kv_append(kc, vc, w.slot_mapping, w.k_new, w.v_new)
+    used = np.zeros((w.num_blocks, 16), bool)
+    for r, c in enumerate(w.context_lens):
+        for t in range(int(c)):
+            used[w.block_tables[r, t // 16], t % 16] = True
+    kc.transpose(0, 2, 1, 3)[~used] = NAN_BF16
+    vc.transpose(0, 2, 1, 3)[~used] = NAN_BF16
+    return W.Workload(**{**w.__dict__, "k_cache": kc, "v_cache": vc})
+
+
+@pytest.mark.parametrize("pbps,sbps", [(0, 0), (4, 0), (0, 8), (8, 16), (12, 1000), (4, 3)])
+def test_cascade_large_batch_with_nan_in_unused_slots(pbps, sbps):
+    # suffix splits merged in a cluster (prefix folded in), or more than 8
+    # splits through workspace slots and the combine pass
+    w, gs, gb, sp = large_cascade_batch(seed=53)
+    w2 = nan_unused(w)
+    out = bf16_to_f64(run_cascade(w2, gs, gb, sp, pbps, sbps, append=False))
+    assert not out[w.context_lens == 0].any()
+    assert_close(out, oracle.run_workload(w2, append=False), what=f"large cascade pbps={pbps} sbps={sbps}")
+
+
+def test_cascade_large_batch_append_and_placement_invariance():
+    w, gs, gb, sp = large_cascade_batch(seed=54, prefix_blocks=20)
+    a = run_cascade(w, gs, gb, sp)
+    assert_close(bf16_to_f64(a), oracle.run_workload(w), what="large cascade append+attention")
+    perm = np.random.default_rng(8).permutation(w.num_blocks)
+    inv = np.argsort(perm)
+    w2 = W.Workload(**{**w.__dict__, "k_cache": np.ascontiguousarray(w.k_cache[perm]),
+                       "v_cache": np.ascontiguousarray(w.v_cache[perm]),
+                       "block_tables": inv[w.block_tables].astype(np.int32),
+                       "slot_mapping": np.where(w.slot_mapping >= 0,
+                                                inv[w.slot_mapping // 16] * 16 + w.slot_mapping % 16, -1)})
+    assert torch.equal(a, run_cascade(w2, gs, gb, sp))
+
+
+def test_cascade_peaky_logits():
+    w, gs, gb, sp = large_cascade_batch(seed=55)
+    w.q = W.bf16_bits((w.q.astype(np.uint32) << 16).view(np.float32) * 8.0)
+    for pbps, sbps in ((0, 0), (8, 16)):
+        assert_close(bf16_to_f64(run_cascade(w, gs, gb, sp, pbps, sbps)), oracle.run_workload(w),
+                     what=f"cascade peaky pbps={pbps} sbps={sbps}")
