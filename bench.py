@@ -390,7 +390,8 @@ def main():
                           device=dev)
         gs_d, gb_d, sp_d = (torch.from_numpy(x).to(dev) for x in (gs_h, gb_h, sp_h))
         splits = -(-maxp // pbps) + -(-maxs // sbps)
-        launches_per_layer = 1 + 3
+        # append, prefix pass, suffix decode (+ the combine pass past 8 suffix splits)
+        launches_per_layer = 1 + 2 + (1 if -(-maxs // sbps) > 8 else 0)
 
     def check(st, what):
         if st != 0:
@@ -402,6 +403,11 @@ def main():
                      kn.data_ptr() + l * kn_stride, vn.data_ptr() + l * kn_stride, t_tok, sp), "kv_append")
         if ev is not None:
             ev[0].record(stream)
+        attention_call(l)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def attention_call(l):
         if q8:
             attn = lib.pkv_paged_attention_fp8_e4m3 if fp8 else lib.pkv_paged_attention_q8_0
             check(attn(out.data_ptr() + l * q_stride, q.data_ptr() + l * q_stride, kp0 + l * pool_stride,
@@ -418,8 +424,6 @@ def main():
                                           kp0 + l * pool_stride, vp0 + l * pool_stride, ctypes.byref(desc),
                                           tables.data_ptr(), maxb, ctx.data_ptr(), b, ql, hq, w.scale, bps,
                                           ws.data_ptr(), ws.numel(), sp), "paged_attention")
-        if ev is not None:
-            ev[1].record(stream)
 
     def step(events=None):
         for l in range(layers):
@@ -470,9 +474,37 @@ def main():
         step(attn_events[s])
     torch.cuda.synchronize()
     attn_ms = [e[0].elapsed_time(e[1]) for st in attn_events for e in st]
-    attn_us = statistics.mean(attn_ms) * 1e3
+    attn_us_isolated = statistics.mean(attn_ms) * 1e3
     if pkv.get_device_error(reset=True) != 0:
         raise RuntimeError("device error word set during the kernel-timing pass")
+
+    # ---- kernel timing, sustained: the layers' attention calls alone, back to
+    # back in one CUDA graph as in the step (launch gaps hidden by programmatic
+    # dependent launch; each call still waits for the previous one before it
+    # reads its inputs), timed with one event pair over K replays ----
+    attn_us = attn_us_isolated
+    sustained = graph is not None
+    if sustained:
+        def attention_layers():
+            for l in range(layers):
+                attention_call(l)
+        attention_layers()
+        torch.cuda.synchronize()
+        attn_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(attn_graph, stream=stream):
+            attention_layers()
+        for _ in range(args.warmup):
+            attn_graph.replay()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a0.record(stream)
+        for _ in range(args.steps):
+            attn_graph.replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        attn_us = a0.elapsed_time(a1) * 1e3 / (args.steps * layers)
+        if pkv.get_device_error(reset=True) != 0:
+            raise RuntimeError("device error word set during the sustained kernel-timing pass")
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -563,6 +595,7 @@ def main():
                        2 * k_pool.numel() * k_pool.element_size() / 1e9),
                    "parallelism": f"replicas x{world}"},
         "us_per_layer_call": round(attn_us, 3),
+        "us_per_layer_call_isolated": round(attn_us_isolated, 3),
         "attention_tokens_layers_per_s": round(world * tokens_layers / (ms_per_step * 1e-3), 1),
         "decode_steps_per_s": round(1e3 / ms_per_step, 2),
         "bytes_per_step": int(step_bytes),
@@ -575,7 +608,10 @@ def main():
                                     "tensor-core chunk" if ql >= 16 else "decode",
                                     " + combine" if (splits > 8 or (ql >= 16 and splits > 1)) else "")),
                      "algorithmic_bytes_per_launch": int(attn_b),
-                     "timing": "mean CUDA-event time of the call over a second timed pass of the same steps"},
+                     "timing": ("sustained: one CUDA event pair over K replays of a graph of the %d layers' "
+                                "attention calls alone, divided by the calls; us_per_layer_call_isolated = mean "
+                                "event time of each call with events around it, launch gaps included" % layers)
+                     if sustained else "mean CUDA-event time of the call over a second timed pass of the same steps"},
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches_per_layer * layers * args.steps),

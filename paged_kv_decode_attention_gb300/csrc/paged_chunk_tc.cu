@@ -75,6 +75,7 @@ struct TcBars {
   uint64_t s_full[kNB];
   uint64_t p_full[kNB];
   uint64_t o_done[kNB];
+  uint64_t q_full;  // the softmax warps have staged Q
   uint32_t tmem_base;
 };
 static_assert(sizeof(TcBars) <= 256, "barrier area");
@@ -149,7 +150,7 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
     return;
   }
 
-  // ---------------- set-up: barriers, TMEM, Q tile ----------------
+  // ---------------- set-up: barriers, TMEM ----------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
@@ -160,6 +161,7 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       mbar_init(&bars->p_full[s], 128);
       mbar_init(&bars->o_done[s], 1);
     }
+    mbar_init(&bars->q_full, 128);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -169,33 +171,6 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
   if (warp == 0 && lane == 0) {
     tc::prefetch_tensor_map(&k_map);
     tc::prefetch_tensor_map(&v_map);
-  }
-  if (warp >= 2) {
-    // Q rows (position, head) -> 128-byte swizzled K-major tile, two 64-dim halves
-    // thread t loads 16-byte chunk t % 16 of rows t / 16 + 8k, k < 8: all
-    // loads issued before the first store, so the (member, query) load chain
-    // costs two round trips, not eight
-    const int t = threadIdx.x - 64;  // 0..127
-    const int ch = t & 15;           // 16-byte chunk of the row
-    const uint16_t* qbase = static_cast<const uint16_t*>(a.q);
-    constexpr int kPerThread = kRows * 16 / 128;
-    uint4 v[kPerThread];
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-      const int m = (t >> 4) + 8 * k;
-      const int ipm = row_pos(m);
-      const int rm = row_req(m);
-      v[k] = make_uint4(0, 0, 0, 0);
-      if (rm >= 0 && ipm < a.q_len)
-        v[k] = *reinterpret_cast<const uint4*>(
-            qbase + ((static_cast<int64_t>(rm) * a.q_len + ipm) * hq + kvh * kGroup + (m & 3)) * kHeadDim + ch * 8);
-    }
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-      const int m = (t >> 4) + 8 * k;
-      *reinterpret_cast<uint4*>(smem + kOffQ + (ch >> 3) * 8192 + tc::sw128_offset(m, (ch & 7) * 8)) = v[k];
-    }
-    tc::fence_proxy_async_smem();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -260,7 +235,8 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       // issues whichever is ready, so neither waits behind the other.
       int js = 0, jp = 0;
       uint64_t t_idle = 0;
-      while (jp < n_tiles) {
+      ok = mbar_wait(&bars->q_full, 0);  // Q staged while the first K/V tiles are in flight
+      while (ok && jp < n_tiles) {
         bool progressed = false;
         if (js < n_tiles) {
           const int st = js % kTcStages, sb = js % kNB;
@@ -312,6 +288,36 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
     __syncwarp();
   } else {
     // ---------------------------- softmax ----------------------------
+    {
+      // Q rows (position, head) -> 128-byte swizzled K-major tile, two 64-dim
+      // halves, staged here rather than before the producer starts so that
+      // these loads overlap the first K/V tiles' flight.  Thread t loads
+      // 16-byte chunk t % 16 of rows t / 16 + 8k, k < 8, all loads issued
+      // before the first store: the (member, query) chain costs two round
+      // trips, not eight.
+      const int t = threadIdx.x - 64;  // 0..127
+      const int ch = t & 15;           // 16-byte chunk of the row
+      const uint16_t* qbase = static_cast<const uint16_t*>(a.q);
+      constexpr int kPerThread = kRows * 16 / 128;
+      uint4 v[kPerThread];
+#pragma unroll
+      for (int k = 0; k < kPerThread; ++k) {
+        const int m = (t >> 4) + 8 * k;
+        const int ipm = row_pos(m);
+        const int rm = row_req(m);
+        v[k] = make_uint4(0, 0, 0, 0);
+        if (rm >= 0 && ipm < a.q_len)
+          v[k] = *reinterpret_cast<const uint4*>(
+              qbase + ((static_cast<int64_t>(rm) * a.q_len + ipm) * hq + kvh * kGroup + (m & 3)) * kHeadDim + ch * 8);
+      }
+#pragma unroll
+      for (int k = 0; k < kPerThread; ++k) {
+        const int m = (t >> 4) + 8 * k;
+        *reinterpret_cast<uint4*>(smem + kOffQ + (ch >> 3) * 8192 + tc::sw128_offset(m, (ch & 7) * 8)) = v[k];
+      }
+      tc::fence_proxy_async_smem();
+      mbar_arrive(&bars->q_full);
+    }
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     // keys this row may see inside this split: causal limit, context, and the
     // split's own block range (the tail tile's extra blocks arrive zero-filled)
