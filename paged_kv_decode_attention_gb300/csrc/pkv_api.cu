@@ -489,7 +489,12 @@ pkv_status quantised_attention(void* out, const void* q, const void* k_cache, co
   const int sms = device_sm_count();
   const int32_t grid = static_cast<int32_t>(units < sms ? units : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (splits == 1) return launch_paged_decode_q8(a, grid, fp8, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  // E4M3 tiles feed the tensor cores' 8-bit path as they are; q8_0 codes are
+  // dequantised inside the kernel
+  auto launch = [&]() {
+    return fp8 ? launch_paged_decode_fp8_tc(a, grid, s) : launch_paged_decode_q8(a, grid, false, s);
+  };
+  if (splits == 1) return launch() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
   const size_t need = pkv_workspace_size_q8_0(num_seqs, num_q_heads, max_blocks_per_seq, bps);
   if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
@@ -497,7 +502,7 @@ pkv_status quantised_attention(void* out, const void* q, const void* k_cache, co
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                         align_up(rows * splits * kHeadDim * sizeof(float), 256));
-  if (launch_paged_decode_q8(a, grid, fp8, s) != cudaSuccess) return PKV_ERR_CUDA;
+  if (launch() != cudaSuccess) return PKV_ERR_CUDA;
   return launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), splits, s) ==
                  cudaSuccess
              ? PKV_OK

@@ -116,6 +116,9 @@ cudaError_t launch_paged_chunk_tc(const ChunkArgs& a, int32_t grid_x, cudaStream
 // of 16 rows x 64 elements with the 128-byte swizzle (paged_chunk_tc.cu).
 bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows);
 
+// Tensor map over an E4M3 KV pool viewed as `rows` rows of 128 bytes, boxes
+// of 16 rows x 128 bytes with the 128-byte swizzle (paged_chunk_tc.cu).
+bool make_pool_map_e4m3(CUtensorMap* map, const void* pool, int64_t rows);
 // Decode (q_len 1) with QK^T and PV on tensor cores, `grid` persistent CTAs
 // striding over the (request, KV head, split) units; num_splits > 1 writes
 // workspace partials for the combine kernel (paged_decode_tc.cu).
@@ -132,6 +135,11 @@ cudaError_t launch_kv_append_q8(void* k_cache, void* v_cache, int32_t num_blocks
                                 const int64_t* slot_mapping, const void* k_new, const void* v_new,
                                 int32_t num_tokens, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_paged_decode_q8(const DecodeArgs& a, int32_t grid, bool fp8, cudaStream_t stream);
+// Decode (q_len 1) over E4M3 pools with both contractions on the tensor
+// cores' 8-bit path, `grid` persistent CTAs striding over the (request, KV
+// head, split) units; num_splits > 1 writes workspace partials
+// (paged_decode_fp8_tc.cu).
+cudaError_t launch_paged_decode_fp8_tc(const DecodeArgs& a, int32_t grid, cudaStream_t stream);
 // FP8 (E4M3) KV: rounding append (pools of kFp8TileBytes per (block, kv head)).
 cudaError_t launch_kv_append_fp8(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
                                  const int64_t* slot_mapping, const void* k_new, const void* v_new,

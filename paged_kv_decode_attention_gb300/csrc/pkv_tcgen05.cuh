@@ -63,6 +63,25 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
   mma_bf16(d_tmem, a_desc, b_desc, idesc, accumulate);
 }
 
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (type code 0 in
+// both fields), FP32 accumulator.  8-bit operands may be K- or MN-major; the
+// K of one instruction is 32 elements (32 bytes of a 128-byte swizzled row).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem] for 8-bit floating-point operands; issued by one thread.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]: A read from tensor memory (M=64: row m in
 // lane 32*(m/16) + m%16, two BF16 per 32-bit column, k-slice kk at column 8*kk).
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -256,6 +275,11 @@ __device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
 // in the 128-byte swizzled layout; the tile base must be 1024-byte aligned.
 __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t col) {
   return row * 128u + ((((col >> 3) ^ (row & 7u)) & 7u) << 4) + ((col & 7u) << 1);
+}
+
+// The same layout for a 128-column tile of 8-bit elements (one byte per column).
+__host__ __device__ constexpr uint32_t sw128_offset_b8(uint32_t row, uint32_t col) {
+  return row * 128u + ((((col >> 4) ^ (row & 7u)) & 7u) << 4) + (col & 15u);
 }
 
 }  // namespace tc

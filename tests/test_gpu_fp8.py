@@ -191,6 +191,23 @@ def test_fp8_large_queries():
     assert_close(bf16_to_f64(out), oracle_fp8(big, kq, vq, tables, ctx, scale), what="fp8 large q")
 
 
+def test_fp8_query_heads_of_mixed_magnitude():
+    """The tensor cores take each query head as two E4M3 parts under its own
+    power-of-two scale: heads 2^-12 and 2^10 times the usual size (below
+    E4M3's normal range and beyond its largest value), an all-zero head
+    (uniform weights: the mean of the V rows) and an 8x sharper head (peaked
+    weights that move the running maximum often) must all match the oracle."""
+    q, kq, vq, tables, ctx = _ragged(10, [700, 1, 129, 2000, 37], hkv=2)
+    x = (q.astype(np.uint32) << 16).view(np.float32).copy()
+    factors = np.array([2.0 ** -12, 2.0 ** 10, 0.0, 8.0, 1.0, 2.0 ** -3, 3.0, 0.5], np.float32)
+    x *= factors[None, None, :, None]
+    qm = (x.view(np.uint32) >> 16).astype(np.uint16)
+    scale = 128 ** -0.5
+    for bps in (0, 24):
+        out = run_fp8(dev(qm), dev(kq), dev(vq), dev(tables), dev(ctx), scale, bps=bps)
+        assert_close(bf16_to_f64(out), oracle_fp8(qm, kq, vq, tables, ctx, scale), what=f"fp8 mixed heads bps={bps}")
+
+
 def test_fp8_bad_block_id_sets_error():
     q, kq, vq, tables, ctx = _ragged(9, [50, 70], hkv=2)
     tables = tables.copy()
