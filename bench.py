@@ -278,7 +278,7 @@ def main():
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workloads: plain paged attention instead of the cascade call")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "q8_0", "fp8_e4m3"],
-                    help="KV pool format: bf16, q8_0 or fp8_e4m3 (the last two: decode only, dequantising kernel)")
+                    help="KV pool format: bf16, q8_0 or fp8_e4m3 (the last two: decode only)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -317,7 +317,8 @@ def main():
     b, ql, hq, hkv, d = w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim
     maxb = w.max_blocks_per_seq
     if q8:
-        bps = args.kv_blocks_per_split or pkv.choose_kv_blocks_per_split_q8_0(b, hkv, maxb)
+        choose = pkv.choose_kv_blocks_per_split_fp8_e4m3 if fp8 else pkv.choose_kv_blocks_per_split_q8_0
+        bps = args.kv_blocks_per_split or choose(b, hkv, maxb)
     else:
         bps = args.kv_blocks_per_split or pkv.choose_kv_blocks_per_split(b, hkv, ql, maxb)
     bps = min(bps, maxb)
@@ -581,7 +582,9 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": f"{args.kv} KV, f16 tensor-core Q.K, f32 softmax and P.V" if q8 else "bf16",
+        "dtype": ("fp8_e4m3 KV, e4m3 tensor-core Q.K and P.V (query and weights as e4m3 high + low parts), "
+                  "f32 accumulation and softmax" if fp8 else
+                  f"{args.kv} KV, f16 tensor-core Q.K, f32 softmax and P.V" if q8 else "bf16"),
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_seqs": b, "q_len": ql,
                    "layers": layers, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16,
@@ -601,8 +604,9 @@ def main():
         "bytes_per_step": int(step_bytes),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
-                     "kernel": ("paged_attention_%s call (tensor-core dequantising decode%s)" % (
-                                    args.kv, " + combine" if splits > 1 else "") if q8 else
+                     "kernel": ("paged_attention_%s call (%s%s)" % (
+                                    args.kv, "8-bit tensor-core decode" if fp8 else "tensor-core dequantising decode",
+                                    " + combine" if splits > 1 else "") if q8 else
                                 "paged_attention_cascade call (prefix tensor-core pass + suffix decode + combine)"
                                 if cascade else "paged_attention call (%s%s)" % (
                                     "tensor-core chunk" if ql >= 16 else "decode",

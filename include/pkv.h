@@ -354,7 +354,7 @@ pkv_status pkv_kv_append_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc
 
 /*
  * pkv_choose_kv_blocks_per_split_q8_0 -- blocks per split for
- * pkv_paged_attention_q8_0 and pkv_paged_attention_fp8_e4m3: their kernel keeps one persistent CTA per SM, so
+ * pkv_paged_attention_q8_0: its kernel keeps one persistent CTA per SM, so
  * the split count is the one that best balances (request, KV head, split)
  * units over sm_count CTAs (0 = current device), in whole 8-block tiles.
  */
@@ -407,10 +407,19 @@ pkv_status pkv_kv_append_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cache_
                                   int32_t num_tokens, void* stream);
 
 /*
+ * pkv_choose_kv_blocks_per_split_fp8_e4m3 -- blocks per split for
+ * pkv_paged_attention_fp8_e4m3: as pkv_choose_kv_blocks_per_split_q8_0 (one
+ * persistent CTA per SM), in whole 16-block tiles, the unit its kernel reads.
+ */
+int32_t pkv_choose_kv_blocks_per_split_fp8_e4m3(int32_t num_seqs, int32_t num_kv_heads,
+                                                int32_t max_blocks_per_seq, int32_t sm_count);
+
+/*
  * pkv_paged_attention_fp8_e4m3 -- one decode step over E4M3 pools with the
- * query in BF16: out = softmax(scale * q . K^T) V on the stored values.
- * Arguments, split choice (pkv_choose_kv_blocks_per_split_q8_0), workspace
- * (pkv_workspace_size_q8_0) and errors exactly as pkv_paged_attention_q8_0.
+ * query in BF16: out = softmax(scale * q . K^T) V on the stored values
+ * (Ch8 §8.4.4: K and V in FP8, the query in BF16).  Arguments, workspace
+ * (pkv_workspace_size_q8_0) and errors exactly as pkv_paged_attention_q8_0;
+ * kv_blocks_per_split 0 = pkv_choose_kv_blocks_per_split_fp8_e4m3.
  */
 pkv_status pkv_paged_attention_fp8_e4m3(void* out, const void* q, const void* k_cache, const void* v_cache,
                                         const pkv_cache_desc* cache, const int32_t* block_tables,

@@ -24,7 +24,7 @@ __all__ = [
     "cascade_workspace_size", "attn_combine", "workspace_size",
     "choose_kv_blocks_per_split", "get_device_error", "library_path", "lib", "DEVERR_BLOCK_ID",
     "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "Q8_TILE_BYTES", "kv_append_q8_0", "paged_attention_q8_0",
-    "choose_kv_blocks_per_split_q8_0", "workspace_size_q8_0", "copy_blocks_q8_0", "FP8_TILE_BYTES",
+    "choose_kv_blocks_per_split_q8_0", "choose_kv_blocks_per_split_fp8_e4m3", "workspace_size_q8_0", "copy_blocks_q8_0", "FP8_TILE_BYTES",
     "kv_append_fp8_e4m3", "paged_attention_fp8_e4m3", "copy_blocks_fp8_e4m3",
 ]
 
@@ -94,6 +94,8 @@ def _load():
     lib.pkv_kv_append_q8_0.restype = ctypes.c_int
     lib.pkv_choose_kv_blocks_per_split_q8_0.argtypes = [i32, i32, i32, i32]
     lib.pkv_choose_kv_blocks_per_split_q8_0.restype = i32
+    lib.pkv_choose_kv_blocks_per_split_fp8_e4m3.argtypes = [i32, i32, i32, i32]
+    lib.pkv_choose_kv_blocks_per_split_fp8_e4m3.restype = i32
     lib.pkv_workspace_size_q8_0.argtypes = [i32, i32, i32, i32]
     lib.pkv_workspace_size_q8_0.restype = sz
     lib.pkv_paged_attention_q8_0.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32, f32, i32,
@@ -393,6 +395,11 @@ def kv_append_q8_0(k_cache: torch.Tensor, v_cache: torch.Tensor, slot_mapping: t
 def choose_kv_blocks_per_split_q8_0(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int,
                                     sm_count: int = 0) -> int:
     return int(_lib.pkv_choose_kv_blocks_per_split_q8_0(num_seqs, num_kv_heads, max_blocks_per_seq, sm_count))
+
+
+def choose_kv_blocks_per_split_fp8_e4m3(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int,
+                                        sm_count: int = 0) -> int:
+    return int(_lib.pkv_choose_kv_blocks_per_split_fp8_e4m3(num_seqs, num_kv_heads, max_blocks_per_seq, sm_count))
 
 
 def workspace_size_q8_0(num_seqs: int, num_q_heads: int, max_blocks_per_seq: int, kv_blocks_per_split: int) -> int:

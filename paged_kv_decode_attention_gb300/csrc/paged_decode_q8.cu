@@ -1,5 +1,4 @@
-// paged_decode_q8.cu -- decode attention over a q8_0 (or FP8 E4M3) paged KV
-// cache, with the dequantisation inside the kernel: Q.K^T on the
+// paged_decode_q8.cu -- decode attention over a q8_0 paged KV cache, with the dequantisation inside the kernel: Q.K^T on the
 // 5th-generation tensor cores, P.V on the CUDA cores, side by side.
 //
 // What it computes ("Chapter 8: Inference Optimization",
@@ -21,9 +20,6 @@
 //        FP32 -- the codes stay exact (int8 -> FP16) and no scale is rounded.
 //   O += P' . V_codes      on the FP32 pipes (~4 cycles per token): P' = p * sV
 //        per (token, head, group), codes converted exactly to FP32.
-//
-// The same kernel serves FP8 KV (§8.4.4: K and V in FP8, the query in BF16):
-// E4M3 tiles of 2048 bytes, converted exactly to FP16 / FP32, all scales 1.
 //
 // CTA = 15 warps (17 with four producers), one per SM, persistent: it walks
 // work units u = blockIdx.x, + gridDim.x, ... (a unit is one (request, KV
@@ -176,31 +172,6 @@ __device__ __forceinline__ void codes_to_f32(uint32_t w, float2& c01, float2& c2
                                __uint_as_float(__byte_perm(x, kMagic, 0x7653))), bias);
 }
 
-// 4 E4M3 codes -> 4 FP16 values (exact: every E4M3 value is an FP16 value).
-__device__ __forceinline__ uint2 e4m3x4_to_f16(uint32_t w) {
-  uint32_t lo, hi;
-  asm("{\n\t.reg .b16 a, b;\n\t"
-      "mov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-  return make_uint2(lo, hi);
-}
-
-// 8 E4M3 codes -> 8 FP16 values.
-__device__ __forceinline__ uint4 e4m3x8_to_f16(uint2 w) {
-  const uint2 a = e4m3x4_to_f16(w.x), b = e4m3x4_to_f16(w.y);
-  return make_uint4(a.x, a.y, b.x, b.y);
-}
-
-// 4 E4M3 codes -> 4 FP32 values.
-__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float2& c01, float2& c23) {
-  const uint2 h = e4m3x4_to_f16(w);
-  c01 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-  c23 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-}
-
 __device__ __forceinline__ void half4_to_float(uint2 w, float* f) {
   const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
   const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
@@ -225,11 +196,9 @@ __device__ __forceinline__ bool merge_sync(uint64_t* merge, uint32_t& n, int lan
   return ok;
 }
 
-// kQ8: q8_0 tiles (int8 codes + FP16 group scales, 2176 B); otherwise E4M3
-// tiles (2048 B, no scale).  Ring slots keep the 2176-byte stride for both.
-template <bool kQ8>
+// q8_0 tiles: int8 codes + FP16 group scales, 2176 B per (block, KV head).
 __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const DecodeArgs a) {
-  constexpr int kTile = kQ8 ? kQ8TileBytes : kFp8TileBytes;
+  constexpr int kTile = kQ8TileBytes;
   pdl_wait();  // inputs may come from the previous grid (e.g. this step's append)
   pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -410,7 +379,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         // this token's K scales, copied out of the K stage by the dequantisation;
         // read before S is released, which orders the read before the slot's reuse
         float sk[4] = {1.f, 1.f, 1.f, 1.f}, sv[4] = {1.f, 1.f, 1.f, 1.f};
-        if constexpr (kQ8) {
+        {
           const int sks = i % kScaleSlots;
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->sk_full[sks], (i / kScaleSlots) & 1));
           if (!ok) break;
@@ -422,7 +391,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         const int so = (k >> 4) * kQ8TileBytes + kQ8CodeBytes + (k & 15) * 8;
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[vst], (i / kVStages) & 1));
         if (!ok) break;
-        if constexpr (kQ8) half4_to_float(*reinterpret_cast<const uint2*>(rawv + so), sv);
+        half4_to_float(*reinterpret_cast<const uint2*>(rawv + so), sv);
         const bool valid = (x.b0 + j * kQ8TileBlocks) * kBlockSize + k < x.ctx_keys;
 #pragma unroll
         for (int q = 0; q < 4; ++q) sv[q] = valid ? sv[q] : 0.f;  // a slot past the data may hold any bits
@@ -469,7 +438,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         __syncwarp();
         // O += P' V over the warp's 32 tokens: lane = dims 4*lane .. 4*lane+3.
         // Only keys that hold data: in a ragged last tile the other slots may
-        // hold any bits, and an E4M3 NaN pattern times a zero weight is NaN.
+        // hold any bits, and a NaN scale pattern times a zero weight is NaN.
         const int nkeys = x.ctx_keys - (x.b0 + j * kQ8TileBlocks) * kBlockSize - 32 * w;
         const uint8_t* vrow = rawv + (2 * w) * kQ8TileBytes + 4 * lane;
         auto pv_keys = [&](int n) {
@@ -478,10 +447,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
             const uint32_t cw = *reinterpret_cast<const uint32_t*>(vrow + (t >> 4) * kQ8TileBytes + (t & 15) * 128);
             const float4 pv = *reinterpret_cast<const float4*>(pw + p_chunk(t, g_own));
             float2 c01, c23;
-            if constexpr (kQ8)
-              codes_to_f32(cw, c01, c23);
-            else
-              e4m3x4_to_f32(cw, c01, c23);
+            codes_to_f32(cw, c01, c23);
             const float ph[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -575,8 +541,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         const uint8_t* stage = smem + kOffRawK + st * kRawStageBytes;
         // token t128's K scales for the softmax (slot i % 4 was last read by the
         // softmax of tile i-4, which released S(i-4) before QK(i-2) ran)
-        if constexpr (kQ8)
-          *reinterpret_cast<uint2*>(smem + kOffSk + (i % kScaleSlots) * 1024 + t128 * 8) =
+        *reinterpret_cast<uint2*>(smem + kOffSk + (i % kScaleSlots) * 1024 + t128 * 8) =
               *reinterpret_cast<const uint2*>(stage + (t128 >> 4) * kQ8TileBytes + kQ8CodeBytes + (t128 & 15) * 8);
         if (j == 0) {
           // the unit's block-diagonal query operand
@@ -600,10 +565,10 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
           wv[jj] = *reinterpret_cast<const uint2*>(raw + (jj >> 1) * kQ8TileBytes + (jj & 1) * 1024);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj)
-          *reinterpret_cast<uint4*>(dst + jj * 1024) = kQ8 ? codes_to_f16(wv[jj]) : e4m3x8_to_f16(wv[jj]);
+          *reinterpret_cast<uint4*>(dst + jj * 1024) = codes_to_f16(wv[jj]);
         tc::fence_proxy_async_smem();  // the operand tiles are read by the tensor core
         mbar_arrive(&bars->kd_full[b]);
-        if constexpr (kQ8) mbar_arrive(&bars->sk_full[i % kScaleSlots]);
+        mbar_arrive(&bars->sk_full[i % kScaleSlots]);
         mbar_arrive(&bars->k_empty[st]);
       }
     }
@@ -618,7 +583,6 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
   }
 }
 
-template <bool kQ8>
 cudaError_t allow_smem_q8() {
   static bool done[64];
   int dev = 0;
@@ -626,7 +590,7 @@ cudaError_t allow_smem_q8() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev]) {
-    e = cudaFuncSetAttribute(paged_decode_q8_kernel<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ8);
+    e = cudaFuncSetAttribute(paged_decode_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ8);
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
@@ -635,15 +599,12 @@ cudaError_t allow_smem_q8() {
 
 }  // namespace
 
-cudaError_t launch_paged_decode_q8(const DecodeArgs& a, int32_t grid, bool fp8, cudaStream_t stream) {
+cudaError_t launch_paged_decode_q8(const DecodeArgs& a, int32_t grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  cudaError_t e = fp8 ? allow_smem_q8<false>() : allow_smem_q8<true>();
+  cudaError_t e = allow_smem_q8();
   if (e != cudaSuccess) return e;
-  if (fp8)
-    return launch_pdl(paged_decode_q8_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kQ8Threads), kSmemQ8,
-                      stream, 1, a);
-  return launch_pdl(paged_decode_q8_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kQ8Threads), kSmemQ8, stream,
-                    1, a);
+  return launch_pdl(paged_decode_q8_kernel, dim3(static_cast<unsigned>(grid)), dim3(kQ8Threads), kSmemQ8, stream, 1,
+                    a);
 }
 
 }  // namespace pkv

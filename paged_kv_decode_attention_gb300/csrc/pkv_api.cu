@@ -88,18 +88,21 @@ bool decode_on_tensor_cores(int64_t num_seqs, int64_t num_kv_heads, int32_t q_le
 // 8-block tiles): minimise the makespan -- the busiest CTA runs
 // ceil(units / SMs) units, each costing its tiles plus about one tile of
 // pipeline fill and epilogue -- with 2 tiles charged for the combine pass.
-int32_t persistent_blocks_per_split(int64_t rows, int32_t max_blocks_per_seq, int32_t sm_count) {
+int32_t persistent_blocks_per_split(int64_t rows, int32_t max_blocks_per_seq, int32_t sm_count,
+                                    int32_t tile_blocks = 8) {
   int32_t best = max_blocks_per_seq;
   int64_t best_cost = INT64_MAX;
   for (int32_t splits = 1; splits <= 64; ++splits) {
     int32_t bps = (max_blocks_per_seq + splits - 1) / splits;
-    bps = (bps + 7) / 8 * 8;
-    if (splits > 1 && bps < 16) break;
+    bps = (bps + tile_blocks - 1) / tile_blocks * tile_blocks;
+    if (splits > 1 && bps < 2 * tile_blocks) break;
     if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
     const int64_t s_eff = (max_blocks_per_seq + bps - 1) / bps;
     const int64_t units = rows * s_eff;
     const int64_t per_cta = (units + sm_count - 1) / sm_count;
-    const int64_t cost = per_cta * ((bps + 7) / 8 + 1) + (s_eff > 1 ? 2 : 0);
+    // in tiles: the unit's tiles plus about one tile of set-up and drain, and
+    // the combine pass when there is more than one split
+    const int64_t cost = per_cta * ((bps + tile_blocks - 1) / tile_blocks + 1) + (s_eff > 1 ? 2 : 0);
     if (cost < best_cost) {
       best_cost = cost;
       best = bps;
@@ -430,6 +433,14 @@ int32_t pkv_choose_kv_blocks_per_split_q8_0(int32_t num_seqs, int32_t num_kv_hea
   return persistent_blocks_per_split(rows, max_blocks_per_seq, sm_count);
 }
 
+int32_t pkv_choose_kv_blocks_per_split_fp8_e4m3(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
+                                                int32_t sm_count) {
+  if (max_blocks_per_seq <= 0) return 1;
+  if (sm_count <= 0) sm_count = device_sm_count();
+  const int64_t rows = static_cast<int64_t>(num_seqs > 0 ? num_seqs : 1) * (num_kv_heads > 0 ? num_kv_heads : 1);
+  return persistent_blocks_per_split(rows, max_blocks_per_seq, sm_count, 16);
+}
+
 size_t pkv_workspace_size_q8_0(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
                                int32_t kv_blocks_per_split) {
   if (num_seqs <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || kv_blocks_per_split <= 0 ||
@@ -463,7 +474,9 @@ pkv_status quantised_attention(void* out, const void* q, const void* k_cache, co
     return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * kBlockSize > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
   int32_t bps = kv_blocks_per_split;
-  if (bps == 0) bps = pkv_choose_kv_blocks_per_split_q8_0(num_seqs, cache->num_kv_heads, max_blocks_per_seq, 0);
+  if (bps == 0)
+    bps = fp8 ? pkv_choose_kv_blocks_per_split_fp8_e4m3(num_seqs, cache->num_kv_heads, max_blocks_per_seq, 0)
+              : pkv_choose_kv_blocks_per_split_q8_0(num_seqs, cache->num_kv_heads, max_blocks_per_seq, 0);
   if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
   const int32_t splits = (max_blocks_per_seq + bps - 1) / bps;
   const int64_t units = static_cast<int64_t>(num_seqs) * cache->num_kv_heads * splits;
@@ -492,7 +505,7 @@ pkv_status quantised_attention(void* out, const void* q, const void* k_cache, co
   // E4M3 tiles feed the tensor cores' 8-bit path as they are; q8_0 codes are
   // dequantised inside the kernel
   auto launch = [&]() {
-    return fp8 ? launch_paged_decode_fp8_tc(a, grid, s) : launch_paged_decode_q8(a, grid, false, s);
+    return fp8 ? launch_paged_decode_fp8_tc(a, grid, s) : launch_paged_decode_q8(a, grid, s);
   };
   if (splits == 1) return launch() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
   const size_t need = pkv_workspace_size_q8_0(num_seqs, num_q_heads, max_blocks_per_seq, bps);

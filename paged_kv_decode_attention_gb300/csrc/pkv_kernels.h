@@ -130,11 +130,10 @@ constexpr int kCascadeGroup = 16;
 // q8_0 KV (pools of kQ8TileBytes per (block, kv head)): quantising append,
 // and decode (q_len 1) on tensor cores, `grid` persistent CTAs walking the
 // (request, KV head, split) units; num_splits > 1 writes workspace partials.
-// fp8 = true runs the same decode over E4M3 pools.
 cudaError_t launch_kv_append_q8(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
                                 const int64_t* slot_mapping, const void* k_new, const void* v_new,
                                 int32_t num_tokens, unsigned int* err, cudaStream_t stream);
-cudaError_t launch_paged_decode_q8(const DecodeArgs& a, int32_t grid, bool fp8, cudaStream_t stream);
+cudaError_t launch_paged_decode_q8(const DecodeArgs& a, int32_t grid, cudaStream_t stream);
 // Decode (q_len 1) over E4M3 pools with both contractions on the tensor
 // cores' 8-bit path, `grid` persistent CTAs striding over the (request, KV
 // head, split) units; num_splits > 1 writes workspace partials

@@ -123,6 +123,10 @@ def test_q8_split_heuristic_and_workspace_are_host_arithmetic():
     bps = lib.pkv_choose_kv_blocks_per_split_q8_0(2, 8, 528, 152)
     assert 16 <= bps < 528 and bps % 8 == 0
     assert lib.pkv_workspace_size_q8_0(37, 32, 144, 144) == 0
+    # the E4M3 kernel reads 16-block tiles: splits in whole 16-block tiles, at least 32 blocks each
+    assert lib.pkv_choose_kv_blocks_per_split_fp8_e4m3(37, 8, 144, 152) == 144
+    bps8 = lib.pkv_choose_kv_blocks_per_split_fp8_e4m3(2, 8, 528, 152)
+    assert 32 <= bps8 < 528 and bps8 % 16 == 0
     rows, splits = 2 * 32, -(-528 // bps)
     o_bytes = -(-rows * splits * 128 * 4 // 256) * 256
     l_bytes = -(-rows * splits * 4 // 256) * 256

@@ -44,7 +44,7 @@ def run_fp8(q, kq, vq, tables, ctx, scale, bps=0):
     b = ctx.shape[0]
     maxb = tables.shape[1]
     if bps == 0:
-        bps = pkv.choose_kv_blocks_per_split_q8_0(b, kq.shape[1], maxb)
+        bps = pkv.choose_kv_blocks_per_split_fp8_e4m3(b, kq.shape[1], maxb)
     ws = torch.empty(max(pkv.workspace_size_q8_0(b, q.shape[2], maxb, bps), 1), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(q)
     pkv.paged_attention_fp8_e4m3(out, q, kq, vq, tables, ctx, scale, kv_blocks_per_split=bps, workspace=ws)
