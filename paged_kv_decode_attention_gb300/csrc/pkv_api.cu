@@ -77,11 +77,42 @@ constexpr int kTcMinBlocksPerSplit = 128;
 // on the persistent tensor-core kernel: with two CTAs per SM already busy,
 // one CTA streaming 192 KiB of tiles per SM wastes less on per-CTA fill and
 // drain (measured: 64 x 32K tokens 0.98 vs 0.88 of the HBM peak, 512 x 512
-// 0.89 vs 0.80); smaller batches keep the CTA-per-row kernel.
+// 0.89 vs 0.80).
 constexpr int kTcDecodeRowsPerSm = 2;
+// Smaller batches go there too when the CTA-per-row kernel's one wave would
+// leave more than a tenth of its slots (2 CTAs per SM) empty -- its CTAs each
+// stream at a fixed rate, so empty slots are lost bandwidth -- provided there
+// are at least 3/4 of a row per SM and requests of at least 128 blocks, where
+// the persistent kernel's larger fixed cost is paid back.  Measured (fraction
+// of the HBM peak, CTA-per-row vs persistent): 24 x 8K tokens 0.66 vs 0.89,
+// 16 x 16K 0.91 vs 0.94, 32 x 32K 0.91 vs 1.01; 8 x 8K (a quarter row per SM)
+// 0.77 vs 0.77; 37 x 2K (97 % of the slots filled) 0.86 vs 0.81.
+constexpr int kTcDecodeMinBlocks = 128;
 
-bool decode_on_tensor_cores(int64_t num_seqs, int64_t num_kv_heads, int32_t q_len, int sm_count) {
-  return q_len == 1 && num_seqs * num_kv_heads >= static_cast<int64_t>(kTcDecodeRowsPerSm) * sm_count;
+// Blocks per split of the CTA-per-row decode kernel: splits are made only
+// when the un-split grid would leave the GPU under-filled, as many as fit in
+// one wave -- a few CTAs spilling into a second wave would double the call's
+// time -- each of at least kMinBlocksPerSplit blocks.
+int32_t row_kernel_blocks_per_split(int64_t rows, int32_t max_blocks_per_seq, int32_t sm_count) {
+  const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
+  if (rows <= 0 || max_blocks_per_seq <= kMinBlocksPerSplit) return max_blocks_per_seq;
+  const int64_t splits = slots / rows;
+  if (splits <= 1) return max_blocks_per_seq;
+  int64_t bps = (max_blocks_per_seq + splits - 1) / splits;
+  if (bps < kMinBlocksPerSplit) bps = kMinBlocksPerSplit;
+  if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
+  return static_cast<int32_t>(bps);
+}
+
+bool decode_on_tensor_cores(int64_t num_seqs, int64_t num_kv_heads, int32_t q_len, int32_t max_blocks_per_seq,
+                            int sm_count) {
+  if (q_len != 1) return false;
+  const int64_t rows = num_seqs * num_kv_heads;
+  if (rows >= static_cast<int64_t>(kTcDecodeRowsPerSm) * sm_count) return true;
+  if (4 * rows < 3 * static_cast<int64_t>(sm_count) || max_blocks_per_seq < kTcDecodeMinBlocks) return false;
+  const int32_t bps = row_kernel_blocks_per_split(rows, max_blocks_per_seq, sm_count);
+  const int64_t ctas = rows * ((max_blocks_per_seq + bps - 1) / bps);
+  return 10 * ctas < 9 * static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
 }
 
 // Split size for the persistent kernels (one CTA per SM walking units of
@@ -159,18 +190,9 @@ int32_t pkv_choose_kv_blocks_per_split(int32_t num_seqs, int32_t num_kv_heads, i
   }
   if (sm_count <= 0) sm_count = device_sm_count();
   const int64_t rows = static_cast<int64_t>(num_seqs) * (q_len > 0 ? q_len : 1) * num_kv_heads;
-  if (decode_on_tensor_cores(num_seqs, num_kv_heads, q_len, sm_count))
+  if (decode_on_tensor_cores(num_seqs, num_kv_heads, q_len, max_blocks_per_seq, sm_count))
     return persistent_blocks_per_split(rows, max_blocks_per_seq, sm_count);
-  const int64_t slots = static_cast<int64_t>(kResidentCtasPerSm) * sm_count;
-  if (rows <= 0 || max_blocks_per_seq <= kMinBlocksPerSplit) return max_blocks_per_seq;
-  // as many splits as fit in one wave: a few CTAs spilling into a second wave
-  // would double the call's time
-  const int64_t splits = slots / rows;
-  if (splits <= 1) return max_blocks_per_seq;
-  int64_t bps = (max_blocks_per_seq + splits - 1) / splits;
-  if (bps < kMinBlocksPerSplit) bps = kMinBlocksPerSplit;
-  if (bps > max_blocks_per_seq) bps = max_blocks_per_seq;
-  return static_cast<int32_t>(bps);
+  return row_kernel_blocks_per_split(rows, max_blocks_per_seq, sm_count);
 }
 
 size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, int32_t head_dim,
@@ -180,7 +202,7 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, 
     return 0;
   const size_t splits = (static_cast<size_t>(max_blocks_per_seq) + kv_blocks_per_split - 1) / kv_blocks_per_split;
   if (q_len < kTcMinQLen && splits <= static_cast<size_t>(kMaxClusterSplits) &&
-      !decode_on_tensor_cores(num_seqs, num_q_heads / kGroup, q_len, device_sm_count()))
+      !decode_on_tensor_cores(num_seqs, num_q_heads / kGroup, q_len, max_blocks_per_seq, device_sm_count()))
     return 0;  // decode splits merge inside a thread-block cluster
   const size_t rows = static_cast<size_t>(num_seqs) * q_len * num_q_heads;
   return align_up(rows * splits * head_dim * sizeof(float), 256) + align_up(rows * splits * sizeof(float), 256);
@@ -232,7 +254,7 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int sms = device_sm_count();
-  if (decode_on_tensor_cores(num_seqs, cache->num_kv_heads, q_len, sms)) {
+  if (decode_on_tensor_cores(num_seqs, cache->num_kv_heads, q_len, max_blocks_per_seq, sms)) {
     const int64_t units = static_cast<int64_t>(num_seqs) * cache->num_kv_heads * splits;
     if (units > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     const int32_t grid = static_cast<int32_t>(units < sms ? units : sms);
@@ -286,9 +308,9 @@ void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups
     pbps = ((pbps + 3) / 4) * 4;  // whole 4-block tiles
     if (pbps < 16) pbps = 16;
   }
-  // suffix pass: the decode heuristic over the longest suffix
+  // suffix pass: the CTA-per-row decode kernel's split over the longest suffix
   const int32_t span = max_suffix_blocks > 0 ? max_suffix_blocks : 1;
-  int32_t sbps = pkv_choose_kv_blocks_per_split(num_seqs, num_kv_heads, 1, span, sm_count);
+  int32_t sbps = row_kernel_blocks_per_split(static_cast<int64_t>(num_seqs) * num_kv_heads, span, sm_count);
   if (prefix_blocks_per_split) *prefix_blocks_per_split = pbps;
   if (suffix_blocks_per_split) *suffix_blocks_per_split = sbps;
 }

@@ -50,11 +50,17 @@ def test_workspace_size_and_split_heuristic_are_host_arithmetic():
     assert need == o_bytes + l_bytes
     # a full GPU needs no split; a small batch over a long context does
     assert lib.pkv_choose_kv_blocks_per_split(512, 8, 1, 144, 152) == 144
-    bps = lib.pkv_choose_kv_blocks_per_split(16, 8, 1, 528, 152)
+    bps = lib.pkv_choose_kv_blocks_per_split(4, 8, 1, 528, 152)
     assert 16 <= bps < 528
     assert lib.pkv_choose_kv_blocks_per_split(1, 8, 1, 8, 152) == 8
     # the split never goes below 16 blocks
     assert lib.pkv_choose_kv_blocks_per_split(1, 1, 1, 4096, 152) >= 16
+    # 24 requests (192 rows) would fill 192 of the CTA-per-row kernel's 304 slots: the persistent
+    # tensor-core kernel takes them, split by its makespan model in 8-block tiles (3 x 48 blocks)
+    assert lib.pkv_choose_kv_blocks_per_split(24, 8, 1, 144, 152) == 48
+    # 37 requests fill 296 of 304 slots: CTA-per-row, no split; short requests stay there too
+    assert lib.pkv_choose_kv_blocks_per_split(37, 8, 1, 144, 152) == 144
+    assert lib.pkv_choose_kv_blocks_per_split(24, 8, 1, 64, 152) == 64
 
 
 def _desc(**kw):

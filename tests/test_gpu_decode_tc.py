@@ -60,6 +60,21 @@ def ragged_contexts(n, seed):
     return ctx
 
 
+@pytest.mark.parametrize("num_seqs,lo,hi", [(24, 2048, 2304), (16, 3000, 4200), (34, 1900, 2100)])
+def test_mid_batch_that_would_underfill_the_row_kernel(num_seqs, lo, hi):
+    """Batches of 3/4 to 2 rows per SM whose CTA-per-row plan leaves more than a
+    tenth of its slots empty also run on the persistent tensor-core kernel
+    (split by its makespan model): same bar against the oracle."""
+    rng = np.random.default_rng(num_seqs)
+    ctx = rng.integers(lo, hi, size=num_seqs)
+    ctx[0] = hi  # the longest request sets the block count the dispatch reads
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("tc-mid", ctx, need + 40, seed=num_seqs)
+    bps = pkv.choose_kv_blocks_per_split(w.num_seqs, w.num_kv_heads, 1, w.max_blocks_per_seq)
+    assert bps % 8 == 0 or bps == w.max_blocks_per_seq  # the persistent kernel's split, in whole tiles
+    assert_close(bf16_to_f64(run(w)), oracle.run_workload(w), what=f"tc mid batch {num_seqs}")
+
+
 @pytest.mark.parametrize("bps", [0, 8, 24, 5, 1000])
 def test_big_batch_ragged_with_nan_in_unused_slots(bps):
     ctx = ragged_contexts(big_batch_rows() + 9, seed=21)
