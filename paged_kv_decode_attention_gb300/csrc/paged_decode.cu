@@ -105,45 +105,57 @@ __device__ __forceinline__ void unpack8x2(const uint4 v, float2* f) {
 
 constexpr float kLog2eF = 1.4426950408889634f;
 
-// Fold the cascade prefix pass's partials of one output row into a running
-// (max in base-2 logits, weight sum, un-normalised dims d0..d0+3).  A partial
-// (normalised O_s, natural-log lse_s) is a block of total weight 1 at the
-// base-2 logit lse_s * log2 e.  The slots are read 8 at a time with every
-// load issued before the first is used.
-__device__ __forceinline__ void fold_prefix(const DecodeArgs& a, int64_t orow, int d0, float& mx, float& sum,
-                                            float* o) {
-  constexpr int kChunk = 8;
+// The cascade prefix pass's partials of one output row, folded into a
+// running (max in base-2 logits, weight sum, un-normalised dims d0..d0+3).  A
+// partial (normalised O_s, natural-log lse_s) is a block of total weight 1 at
+// the base-2 logit lse_s * log2 e.  The slots are read kPrefixChunk at a time
+// with every load issued before the first is used.
+constexpr int kPrefixChunk = 8;
+
+__device__ __forceinline__ void load_prefix_chunk(const DecodeArgs& a, int64_t orow, int d0, int s0, float* ls,
+                                                  float4* v) {
   const int ns = a.prefix_slots;
   const float* lse = a.prefix_lse + orow * ns;
   const float* po = a.prefix_o + orow * ns * kHeadDim + d0;
-  for (int s0 = 0; s0 < ns; s0 += kChunk) {
-    float ls[kChunk];
-    float4 v[kChunk];
 #pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-      const int sl = s0 + k;
-      ls[k] = sl < ns ? lse[sl] * kLog2eF : -INFINITY;
-      v[k] = sl < ns ? *reinterpret_cast<const float4*>(po + sl * kHeadDim) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float m2 = mx;
+  for (int k = 0; k < kPrefixChunk; ++k) {
+    const int sl = s0 + k;
+    ls[k] = sl < ns ? lse[sl] * kLog2eF : -INFINITY;
+    v[k] = sl < ns ? *reinterpret_cast<const float4*>(po + sl * kHeadDim) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+__device__ __forceinline__ void fold_prefix_chunk(const float* ls, const float4* v, float& mx, float& sum,
+                                                  float* o) {
+  float m2 = mx;
 #pragma unroll
-    for (int k = 0; k < kChunk; ++k) m2 = fmaxf(m2, ls[k]);
-    if (m2 == -INFINITY) continue;
-    const float sc_old = exp2_approx(mx - m2);  // 0 when nothing was accumulated yet
-    sum *= sc_old;
+  for (int k = 0; k < kPrefixChunk; ++k) m2 = fmaxf(m2, ls[k]);
+  if (m2 == -INFINITY) return;
+  const float sc_old = exp2_approx(mx - m2);  // 0 when nothing was accumulated yet
+  sum *= sc_old;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] *= sc_old;
+  for (int e = 0; e < 4; ++e) o[e] *= sc_old;
 #pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-      if (ls[k] == -INFINITY) continue;  // an empty prefix split: its output is never used
-      const float w = exp2_approx(ls[k] - m2);
-      sum += w;
-      o[0] = fmaf(w, v[k].x, o[0]);
-      o[1] = fmaf(w, v[k].y, o[1]);
-      o[2] = fmaf(w, v[k].z, o[2]);
-      o[3] = fmaf(w, v[k].w, o[3]);
-    }
-    mx = m2;
+  for (int k = 0; k < kPrefixChunk; ++k) {
+    if (ls[k] == -INFINITY) continue;  // an empty prefix split: its output is never used
+    const float w = exp2_approx(ls[k] - m2);
+    sum += w;
+    o[0] = fmaf(w, v[k].x, o[0]);
+    o[1] = fmaf(w, v[k].y, o[1]);
+    o[2] = fmaf(w, v[k].z, o[2]);
+    o[3] = fmaf(w, v[k].w, o[3]);
+  }
+  mx = m2;
+}
+
+// Slots s_first.. of the row (all of them by default).
+__device__ __forceinline__ void fold_prefix(const DecodeArgs& a, int64_t orow, int d0, float& mx, float& sum,
+                                            float* o, int s_first = 0) {
+  for (int s0 = s_first; s0 < a.prefix_slots; s0 += kPrefixChunk) {
+    float ls[kPrefixChunk];
+    float4 v[kPrefixChunk];
+    load_prefix_chunk(a, orow, d0, s0, ls, v);
+    fold_prefix_chunk(ls, v, mx, sum, o);
   }
 }
 
@@ -491,9 +503,18 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
   }
 
   if constexpr (kMode == SplitMode::kCluster) {
+    // The leader waits for the prefix pass and issues the loads of its first
+    // partials before the cluster merge, so their latency overlaps the merge.
+    const bool lead = cluster_cta_rank() == 0 && warp < kConsumerWarps;
+    float pre_ls[kPrefixChunk];
+    float4 pre_v[kPrefixChunk];
+    if (has_prefix && lead) {
+      pdl_wait();  // the prefix pass wrote these partials
+      load_prefix_chunk(a, qrow0 + warp, lane * 4, 0, pre_ls, pre_v);
+    }
     // every CTA of the cluster has left its (max, sum, acc) in shared memory
     cluster_sync_all();
-    if (cluster_cta_rank() == 0 && warp < kConsumerWarps) {
+    if (lead) {
       const int h = warp;
       const int d0 = lane * 4;
       const uint32_t nranks = gridDim.y;  // cluster = all splits of this (row, KV head)
@@ -514,9 +535,9 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
         }
       }
       if (has_prefix) {
-        pdl_wait();  // the prefix pass wrote these partials
         float o4[4] = {o0, o1, o2, o3};
-        fold_prefix(a, qrow0 + h, d0, mx, sum, o4);
+        fold_prefix_chunk(pre_ls, pre_v, mx, sum, o4);
+        fold_prefix(a, qrow0 + h, d0, mx, sum, o4, kPrefixChunk);  // slots past the first chunk
         o0 = o4[0];
         o1 = o4[1];
         o2 = o4[2];
