@@ -430,14 +430,25 @@ def main():
         for l in range(layers):
             layer_call(l, None if events is None else events[l])
 
+    # the step as the library's decode graph: one CUDA graph per buffer set
+    # (set 0 = the buffers above, set 1 = a second copy for the end-to-end
+    # leg's ping-pong), each the layers' append + attention calls
     graph = None
+    sets_dev = None
     if args.graph:
-        step()  # warm the library's per-device lookups before capture
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            step()
-        run_step = lambda events=None: graph.replay()
+        sets_dev = [dict(q=q, k_new=kn, v_new=vn, slot_mapping=slots, block_tables=tables, context_lens=ctx, out=out)]
+        sets_dev.append({k: v.clone() for k, v in sets_dev[0].items()})
+        if cascade:
+            for st_ in sets_dev:
+                st_.update(group_seqs=gs_d.clone(), group_blocks=gb_d.clone(), seq_prefix_blocks=sp_d.clone())
+        graph = pkv.DecodeGraph(
+            [kp0 + l * pool_stride for l in range(layers)], [vp0 + l * pool_stride for l in range(layers)], desc,
+            sets_dev, num_seqs=b, q_len=ql, num_q_heads=hq, max_blocks_per_seq=maxb, num_tokens=t_tok,
+            scale=w.scale, kv_format=pkv.KV_FP8_E4M3 if fp8 else pkv.KV_Q8_0 if q8 else pkv.KV_BF16,
+            kv_blocks_per_split=bps, workspace=cws if cascade else ws,
+            cascade={"num_groups": int(gs_h.shape[0]), "max_prefix_blocks": maxp, "max_suffix_blocks": maxs,
+                     "prefix_blocks_per_split": pbps, "suffix_blocks_per_split": sbps} if cascade else None)
+        run_step = lambda events=None: graph.launch(0, stream)
     else:
         run_step = step
 
@@ -516,6 +527,38 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in (p_q, p_kn, p_vn, p_tables, p_ctx, p_slots))
         d2h = p_out.numel() * p_out.element_size()
 
+        def e2e_run_graph(n_steps):
+            """The decode loop with the two buffer sets: step n runs set n % 2
+            while the copy stream uploads step n + 1's inputs into the other
+            set and reads step n's output back; the host waits for step n - 1's
+            output before enqueueing step n + 1 (at most two steps in flight)."""
+            copy = e2e_copy_stream
+            copy.wait_stream(stream)
+            for n in range(n_steps):
+                s_ = n & 1
+                st_ = sets_dev[s_]
+                if n == 0:
+                    with torch.cuda.stream(copy):
+                        for name, src in pinned_in:
+                            st_[name].copy_(src, non_blocking=True)
+                        ev_in[0].record(copy)
+                stream.wait_event(ev_in[s_])
+                graph.launch(s_, stream)
+                ev_done[s_].record(stream)
+                with torch.cuda.stream(copy):
+                    if n + 1 < n_steps:
+                        if n >= 1:
+                            copy.wait_event(ev_done[1 - s_])  # the other set's last step is done
+                        for name, src in pinned_in:
+                            sets_dev[1 - s_][name].copy_(src, non_blocking=True)
+                        ev_in[1 - s_].record(copy)
+                    copy.wait_event(ev_done[s_])
+                    p_outs[s_].copy_(st_["out"], non_blocking=True)
+                    ev_out[s_].record(copy)
+                if n >= 1:
+                    ev_out[1 - s_].synchronize()  # step n - 1's result is on the host
+            ev_out[(n_steps - 1) & 1].synchronize()
+
         def e2e_step():
             for dst, src in ((q, p_q), (kn, p_kn), (vn, p_vn), (tables, p_tables), (ctx, p_ctx), (slots, p_slots)):
                 dst.copy_(src, non_blocking=True)
@@ -536,13 +579,29 @@ def main():
             p_out.copy_(out, non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
-        for _ in range(2):
-            e2e_step()
-        barrier(world)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        el = all_max(time.perf_counter() - t0, world)
+        if graph is not None:
+            e2e_copy_stream = torch.cuda.Stream(dev)
+            pinned_in = [("q", p_q), ("k_new", p_kn), ("v_new", p_vn), ("block_tables", p_tables),
+                         ("context_lens", p_ctx), ("slot_mapping", p_slots)]
+            p_outs = [p_out, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
+            ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+            ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+            ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+            e2e_run_graph(2)
+            torch.cuda.synchronize()
+            barrier(world)
+            t0 = time.perf_counter()
+            e2e_run_graph(args.steps)
+            torch.cuda.synchronize()
+            el = all_max(time.perf_counter() - t0, world)
+        else:
+            for _ in range(2):
+                e2e_step()
+            barrier(world)
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                e2e_step()
+            el = all_max(time.perf_counter() - t0, world)
         e2e = {"value": round(world * step_bytes / (el / args.steps) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(el / args.steps * 1e3, 4), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}

@@ -23,7 +23,8 @@
  *
  * Conventions shared by every entry point:
  *   - All tensors are caller-owned device memory; the library never allocates,
- *     frees or synchronises, and every call only enqueues work on `stream`
+ *     frees or synchronises (pkv_decode_graph_create/_destroy aside: they
+ *     build and free CUDA graphs), and every call only enqueues work on `stream`
  *     (a cudaStream_t passed as void*; NULL is the legacy default stream).
  *   - BF16 values are passed as raw 16-bit patterns (void*).
  *   - Cache layout, per tensor (K and V are separate buffers of identical
@@ -434,6 +435,96 @@ pkv_status pkv_copy_blocks_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cach
 
 /* Human-readable name of a status code (static string). */
 const char* pkv_status_string(pkv_status status);
+
+/*
+ * Decode step as one CUDA graph, with two fixed buffer sets.
+ *
+ * Ch8 §8.6.3 measures decode rounds with CUDA graphs off and traces the
+ * roughly fixed time above the read bound (about 17.6 ms at batch 1) to
+ * submitting kernels one by one from the host, which a CUDA graph removes.
+ * The page "Popping the GPU bubble" (Photon, §3 "ping-pong slots") keeps a
+ * decode step's buffers at fixed addresses, allocated once, so the step can
+ * be captured as a graph, and alternates two such buffer sets so that the
+ * host prepares one step while the GPU runs the other.  A step of L layers
+ * issues L appends and L attention calls; pkv_decode_graph_create captures
+ * that step -- for layer l: the append of the step's new tokens into layer
+ * l's pools, then the attention over them -- once for each of two buffer
+ * sets and instantiates the two graphs; pkv_decode_graph_launch replays one
+ * with a single launch.  While the graph of buffer set s runs, the caller
+ * fills set 1 - s (the next step's queries, new K/V, slots, tables and
+ * lengths), so uploads overlap compute.
+ *
+ * Per buffer set (all device memory, caller-owned, fixed for the graph's
+ * life; the graph reads and writes them at every launch):
+ *   q, out        : BF16 [num_layers][num_seqs][q_len][num_q_heads][128]
+ *   k_new, v_new  : BF16 [num_layers][num_tokens][num_kv_heads][128]
+ *   slot_mapping  : int64 [num_tokens], shared by the layers (<0 = skip)
+ *   block_tables  : int32 [num_seqs][max_blocks_per_seq], shared by the layers
+ *   context_lens  : int32 [num_seqs], shared by the layers
+ *   cascade only  : group_seqs [num_groups][16], group_blocks [num_groups],
+ *                   seq_prefix_blocks [num_seqs] (as pkv_paged_attention_cascade)
+ * Shared by both sets:
+ *   k_caches, v_caches : host arrays of num_layers device pointers, the
+ *                        layers' pools (format kv_format, geometry `cache`)
+ *   workspace          : the attention call's workspace (the graphs run in
+ *                        stream order, so one serves both), sized by
+ *                        pkv_workspace_size / _q8_0 / pkv_cascade_workspace_size
+ * kv_format: PKV_KV_BF16 (pkv_kv_append + pkv_paged_attention, or
+ * pkv_paged_attention_cascade when num_groups > 0), PKV_KV_Q8_0 or
+ * PKV_KV_FP8_E4M3 (their append and decode calls; q_len 1, no groups).
+ * Split sizes as for the direct calls (0 = the library's heuristic).
+ *
+ * Ownership and errors: create validates every call of the step with the
+ * same rules as the direct calls, returning the first failing status and no
+ * graph; it allocates host memory and two CUDA graph executables (the only
+ * entry point that does) and enqueues nothing.  launch enqueues one graph on
+ * `stream` and allocates nothing; buffer_set must be 0 or 1.  destroy frees
+ * both graphs; the caller must not destroy a graph while a launch of it may
+ * still run.  The device error word behaves as for the direct calls.
+ */
+typedef enum pkv_kv_format { PKV_KV_BF16 = 0, PKV_KV_Q8_0 = 1, PKV_KV_FP8_E4M3 = 2 } pkv_kv_format;
+
+typedef struct pkv_decode_graph_buffers {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  const int32_t* group_seqs;
+  const int32_t* group_blocks;
+  const int32_t* seq_prefix_blocks;
+} pkv_decode_graph_buffers;
+
+typedef struct pkv_decode_graph_desc {
+  int32_t num_layers;
+  int32_t kv_format;             /* pkv_kv_format */
+  pkv_cache_desc cache;
+  void* const* k_caches;         /* [num_layers] */
+  void* const* v_caches;         /* [num_layers] */
+  int32_t num_seqs;
+  int32_t q_len;
+  int32_t num_q_heads;
+  int32_t max_blocks_per_seq;
+  int32_t num_tokens;            /* new tokens appended per layer */
+  float scale;
+  int32_t kv_blocks_per_split;   /* non-cascade calls; 0 = heuristic */
+  int32_t num_groups;            /* BF16 decode only: > 0 = cascade */
+  int32_t max_prefix_blocks;
+  int32_t max_suffix_blocks;
+  int32_t prefix_blocks_per_split;
+  int32_t suffix_blocks_per_split;
+  void* workspace;
+  size_t workspace_bytes;
+  pkv_decode_graph_buffers set[2];
+} pkv_decode_graph_desc;
+
+typedef struct pkv_decode_graph pkv_decode_graph; /* opaque */
+
+pkv_status pkv_decode_graph_create(const pkv_decode_graph_desc* desc, pkv_decode_graph** graph);
+pkv_status pkv_decode_graph_launch(pkv_decode_graph* graph, int32_t buffer_set, void* stream);
+void pkv_decode_graph_destroy(pkv_decode_graph* graph);
 
 #ifdef __cplusplus
 }

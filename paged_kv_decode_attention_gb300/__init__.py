@@ -26,6 +26,7 @@ __all__ = [
     "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "Q8_TILE_BYTES", "kv_append_q8_0", "paged_attention_q8_0",
     "choose_kv_blocks_per_split_q8_0", "choose_kv_blocks_per_split_fp8_e4m3", "workspace_size_q8_0", "copy_blocks_q8_0", "FP8_TILE_BYTES",
     "kv_append_fp8_e4m3", "paged_attention_fp8_e4m3", "copy_blocks_fp8_e4m3",
+    "DecodeGraph", "KV_BF16", "KV_Q8_0", "KV_FP8_E4M3",
 ]
 
 DEVERR_BLOCK_ID = 1
@@ -47,6 +48,26 @@ class PkvError(RuntimeError):
 class CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+KV_BF16, KV_Q8_0, KV_FP8_E4M3 = 0, 1, 2
+
+
+class DecodeGraphBuffers(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
+                                               "out", "group_seqs", "group_blocks", "seq_prefix_blocks")]
+
+
+class DecodeGraphDesc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("kv_format", ctypes.c_int32), ("cache", CacheDesc),
+                ("k_caches", ctypes.POINTER(ctypes.c_void_p)), ("v_caches", ctypes.POINTER(ctypes.c_void_p)),
+                ("num_seqs", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("num_tokens", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("kv_blocks_per_split", ctypes.c_int32), ("num_groups", ctypes.c_int32),
+                ("max_prefix_blocks", ctypes.c_int32), ("max_suffix_blocks", ctypes.c_int32),
+                ("prefix_blocks_per_split", ctypes.c_int32), ("suffix_blocks_per_split", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("set", DecodeGraphBuffers * 2)]
 
 
 def _load():
@@ -110,6 +131,12 @@ def _load():
     lib.pkv_paged_attention_fp8_e4m3.restype = ctypes.c_int
     lib.pkv_copy_blocks_fp8_e4m3.argtypes = [p, p, ctypes.POINTER(CacheDesc), p, p, i32, p]
     lib.pkv_copy_blocks_fp8_e4m3.restype = ctypes.c_int
+    lib.pkv_decode_graph_create.argtypes = [ctypes.POINTER(DecodeGraphDesc), ctypes.POINTER(ctypes.c_void_p)]
+    lib.pkv_decode_graph_create.restype = ctypes.c_int
+    lib.pkv_decode_graph_launch.argtypes = [p, i32, p]
+    lib.pkv_decode_graph_launch.restype = ctypes.c_int
+    lib.pkv_decode_graph_destroy.argtypes = [p]
+    lib.pkv_decode_graph_destroy.restype = None
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.pkv_get_device_error.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
@@ -519,6 +546,84 @@ def copy_blocks_fp8_e4m3(k_cache: torch.Tensor, v_cache: torch.Tensor, src_block
     _check(_lib.pkv_copy_blocks_fp8_e4m3(k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
                                          src_blocks.data_ptr(), dst_blocks.data_ptr(), src_blocks.numel(),
                                          _stream_ptr(stream)), "pkv_copy_blocks_fp8_e4m3")
+
+
+def _addr(x) -> int:
+    return int(x) if isinstance(x, int) else int(x.data_ptr())
+
+
+class DecodeGraph:
+    """A decode step of `num_layers` layers -- per layer, the append of the
+    step's new tokens into that layer's pools, then the attention over them --
+    captured once per buffer set as a CUDA graph (pkv_decode_graph_create);
+    launch(s) replays set s with one launch.  Fill one set while the other
+    runs ("ping-pong" buffers).
+
+    k_caches, v_caches: per-layer pools (tensors or device addresses) of
+    format `kv_format` and geometry `cache` (a CacheDesc).  sets: two dicts of
+    contiguous CUDA tensors: q, out (BF16 [num_layers][num_seqs][q_len][Hq][128]),
+    k_new, v_new (BF16 [num_layers][num_tokens][Hkv][128]), slot_mapping
+    (int64), block_tables, context_lens (int32), and for a cascade
+    group_seqs, group_blocks, seq_prefix_blocks (int32).  cascade: None or a
+    dict of num_groups, max_prefix_blocks, max_suffix_blocks and optionally
+    prefix_blocks_per_split, suffix_blocks_per_split.  Buffer extents are
+    the caller's to get right, as for the direct calls."""
+
+    def __init__(self, k_caches, v_caches, cache: CacheDesc, sets, *, num_seqs: int, q_len: int, num_q_heads: int,
+                 max_blocks_per_seq: int, num_tokens: int, scale: float, kv_format: int = KV_BF16,
+                 kv_blocks_per_split: int = 0, workspace: torch.Tensor | None = None, cascade: dict | None = None):
+        self._handle = None
+        if len(sets) != 2 or len(k_caches) != len(v_caches):
+            raise ValueError("two buffer sets and one K and one V pool per layer are required")
+        n = len(k_caches)
+        kc = (ctypes.c_void_p * n)(*[_addr(t) for t in k_caches])
+        vc = (ctypes.c_void_p * n)(*[_addr(t) for t in v_caches])
+        d = DecodeGraphDesc()
+        d.num_layers, d.kv_format, d.cache = n, kv_format, cache
+        d.k_caches = ctypes.cast(kc, ctypes.POINTER(ctypes.c_void_p))
+        d.v_caches = ctypes.cast(vc, ctypes.POINTER(ctypes.c_void_p))
+        d.num_seqs, d.q_len, d.num_q_heads = num_seqs, q_len, num_q_heads
+        d.max_blocks_per_seq, d.num_tokens, d.scale = max_blocks_per_seq, num_tokens, scale
+        d.kv_blocks_per_split = kv_blocks_per_split
+        if cascade:
+            d.num_groups = cascade["num_groups"]
+            d.max_prefix_blocks = cascade["max_prefix_blocks"]
+            d.max_suffix_blocks = cascade["max_suffix_blocks"]
+            d.prefix_blocks_per_split = cascade.get("prefix_blocks_per_split", 0)
+            d.suffix_blocks_per_split = cascade.get("suffix_blocks_per_split", 0)
+        if workspace is not None:
+            d.workspace, d.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+        self._keep = [kc, vc, workspace, sets]
+        for i, st in enumerate(sets):
+            b = d.set[i]
+            for name in ("q", "out"):
+                _bf16(st[name], f"sets[{i}].{name}")
+            for name in ("block_tables", "context_lens") + (
+                    ("group_seqs", "group_blocks", "seq_prefix_blocks") if cascade else ()):
+                _i32(st[name], f"sets[{i}].{name}")
+            if num_tokens > 0:
+                _bf16(st["k_new"], f"sets[{i}].k_new")
+                _bf16(st["v_new"], f"sets[{i}].v_new")
+                if st["slot_mapping"].dtype != torch.int64 or not st["slot_mapping"].is_cuda:
+                    raise ValueError(f"sets[{i}].slot_mapping must be a CUDA int64 tensor")
+            for name, _ in DecodeGraphBuffers._fields_:
+                t = st.get(name)
+                if t is not None:
+                    setattr(b, name, t.data_ptr())
+        h = ctypes.c_void_p()
+        _check(_lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)), "pkv_decode_graph_create")
+        self._handle = h
+
+    def launch(self, buffer_set: int, stream=None) -> None:
+        _check(_lib.pkv_decode_graph_launch(self._handle, buffer_set, _stream_ptr(stream)), "pkv_decode_graph_launch")
+
+    def close(self) -> None:
+        if self._handle is not None:
+            _lib.pkv_decode_graph_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        self.close()
 
 
 def get_device_error(reset: bool = True) -> int:

@@ -190,3 +190,32 @@ def test_fp8_argument_errors():
     assert call() == 4
     assert call(b=0) == 0
     assert lib.pkv_copy_blocks_fp8_e4m3(p, p, d, p, p, 0, None) == 0
+
+
+def test_decode_graph_argument_errors():
+    """pkv_decode_graph_create checks its description on the host and returns
+    before any CUDA call; launch and destroy reject a NULL graph."""
+    lib = pkv.lib()
+    h = ctypes.c_void_p()
+    d = pkv.DecodeGraphDesc()
+    assert lib.pkv_decode_graph_create(None, ctypes.byref(h)) == 1
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), None) == 1
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == 2  # no layers
+    d.num_layers, d.q_len, d.num_q_heads, d.num_seqs, d.num_tokens = 2, 1, 32, 4, 4
+    d.cache = _desc()
+    d.kv_format = 7
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == 3
+    d.kv_format, d.q_len = pkv.KV_Q8_0, 2  # quantised pools: decode only
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == 3
+    d.kv_format, d.q_len, d.num_groups = pkv.KV_FP8_E4M3, 1, 1  # no cascade over quantised pools
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == 3
+    d.kv_format, d.num_groups = pkv.KV_BF16, 0
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == 1  # no pool arrays
+    fake = (ctypes.c_void_p * 2)(4096, 0)
+    d.k_caches = d.v_caches = ctypes.cast(fake, ctypes.POINTER(ctypes.c_void_p))
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == 1  # layer 1 has no pool
+    fake[1] = 8192
+    assert lib.pkv_decode_graph_create(ctypes.byref(d), ctypes.byref(h)) == 1  # buffer sets unset
+    assert not h.value
+    assert lib.pkv_decode_graph_launch(None, 0, None) == 1
+    lib.pkv_decode_graph_destroy(None)
