@@ -129,7 +129,12 @@ __device__ __forceinline__ bool dt_produce(const DecodeArgs& a, const CUtensorMa
     const DtUnit x = dt_unit(a, u);
     if (x.n_tiles == 0) continue;
     const int32_t* table = a.block_tables + static_cast<int64_t>(x.r) * a.max_blocks;
-    auto entry = [&](int bi) -> int { return bi < x.b1 ? table[bi] : INT_MIN; };  // checked where used
+    // the load stays inside the table row whatever the context length, so it
+    // need not wait for that length; entries past the unit's blocks are dropped
+    auto entry = [&](int bi) -> int {
+      const int raw = table[min(bi, a.max_blocks - 1)];
+      return bi < x.b1 ? raw : INT_MIN;  // checked where used
+    };
     int cur = entry(x.b0 + lane);
     int nxt = INT_MIN;
     for (int j = 0; j < x.n_tiles; ++j, ++i) {
@@ -171,7 +176,6 @@ __device__ __forceinline__ float sel4(const float* v, int k) {
 __global__ void __launch_bounds__(kDtThreads, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                            const DecodeArgs a) {
-  pdl_wait();  // inputs come from earlier grids in the stream
   pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem[];
   DtBars* bars = reinterpret_cast<DtBars*>(smem + kOffBar);
@@ -215,6 +219,9 @@ __global__ void __launch_bounds__(kDtThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  // The set-up above reads no input; everything below may read what earlier
+  // grids in the stream write, so wait for them here.
+  pdl_wait();
   const uint32_t tmem = bars->tmem_base;
   const uint32_t sbase = smem_addr(smem);
   bool ok = true;
