@@ -182,6 +182,14 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
   const int i = vrow - r * a.q_len;
   const int hq = a.num_kv_heads * kGroup;
 
+  const int start = a.seq_start_block ? a.seq_start_block[r] : 0;  // blocks before it are reduced elsewhere
+  // The producer's first 32 block ids, loaded before the context length is
+  // known (the load stays inside the table row; ids past the range are dropped
+  // below), so the first copies do not wait for two dependent loads.
+  int first_ids = 0;
+  if (warp == kConsumerWarps)
+    first_ids = a.block_tables[static_cast<int64_t>(r) * a.max_blocks +
+                               max(0, min(start + split * a.blocks_per_split + lane, a.max_blocks - 1))];
   const int ctx = a.context_lens[r];
   int n_vis = ctx - a.q_len + 1 + i;  // keys visible to query i
   if (n_vis > a.max_blocks * kBlockSize) {
@@ -190,7 +198,6 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
   }
   if (ctx <= 0 || n_vis < 0) n_vis = 0;
   const int nb = (n_vis + kBlockSize - 1) / kBlockSize;
-  const int start = a.seq_start_block ? a.seq_start_block[r] : 0;  // blocks before it are reduced elsewhere
   const int b0 = start + split * a.blocks_per_split;
   const int b1 = min(nb, b0 + a.blocks_per_split);
   const int64_t qrow0 = static_cast<int64_t>(vrow) * hq + kvh * kGroup;  // (r, i, first head of group)
@@ -262,7 +269,7 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
         }
         return b;
       };
-      int blk_next = chunk(0);
+      int blk_next = lane < n_iter ? first_ids : INT_MIN;  // chunk(0), loaded at the top
       for (int base = 0; base < n_iter && ok; base += 32) {
         const int blk = checked(blk_next);
         blk_next = chunk(base + 32);  // the next chunk's ids, read while this one streams
