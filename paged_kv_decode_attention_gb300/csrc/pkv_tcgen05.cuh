@@ -3,13 +3,15 @@
 // memory operand descriptors, completion via tcgen05.commit, TMEM <-> register
 // moves, and TMA tiled loads through a tensor map.
 //
-// Operand layouts used by the attention kernels (all BF16, 128-byte swizzle):
-//   K-major operand tile: rows of 64 elements (128 B), 8-row groups of
-//     1024 B; the 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
-//     Descriptor: SBO = 1024 B (next 8-row group), LBO unused, and the k-th
-//     16-element slice starts 32*k bytes into the row.
-//   MN-major operand tile: rows along K of 64 MN-elements (128 B), 8-row
-//     groups of 1024 B (SBO), the next 64 MN-elements LBO bytes further.
+// Operand layouts used by the attention kernels (128-byte swizzle):
+//   K-major operand tile: rows of 128 B (64 BF16 or 128 E4M3 elements),
+//     8-row groups of 1024 B; the 16-byte chunk c of row r sits at chunk
+//     position c ^ (r % 8).  Descriptor: SBO = 1024 B (next 8-row group), LBO
+//     unused, and the k-th K-slice of one MMA (16 BF16 or 32 E4M3 elements,
+//     32 B either way) starts 32*k bytes into the row.
+//   MN-major operand tile: rows along K of 128 B of MN-elements (64 BF16 or
+//     128 E4M3), 8-row groups of 1024 B (SBO), the next 128 B of MN-elements
+//     LBO bytes further.
 #pragma once
 
 #include <cstdint>
