@@ -683,6 +683,27 @@ def main():
     print(json.dumps(line), flush=True)
 
 
+def quantised_pools(pkv, kv: str, nb: int, seed: int, dev, chunk: int = 4096):
+    """K and V pools of `nb` blocks in the q8_0 or E4M3 format, every slot
+    holding N(0,1) BF16 values stored through the format's append, filled
+    `chunk` blocks at a time so the BF16 staging stays small."""
+    fp8 = kv == "fp8_e4m3"
+    tile = (16, 128) if fp8 else (pkv.Q8_TILE_BYTES,)
+    kq = torch.empty((nb, 8) + tile, dtype=torch.uint8, device=dev)
+    vq = torch.empty_like(kq)
+    append = pkv.kv_append_fp8_e4m3 if fp8 else pkv.kv_append_q8_0
+    tk = torch.empty((min(chunk, nb), 8, 16, 128), dtype=torch.bfloat16, device=dev)
+    tv = torch.empty_like(tk)
+    for c0 in range(0, nb, chunk):
+        n = min(chunk, nb - c0)
+        W.fill_pool_device(tk[:n], seed * 7919 + 2 * c0)
+        W.fill_pool_device(tv[:n], seed * 7919 + 2 * c0 + 1)
+        slots = torch.arange(c0 * 16, (c0 + n) * 16, dtype=torch.int64, device=dev)
+        append(kq, vq, slots, tk[:n].permute(0, 2, 1, 3).contiguous().view(n * 16, 8, 128),
+               tv[:n].permute(0, 2, 1, 3).contiguous().view(n * 16, 8, 128))
+    return kq, vq
+
+
 def run_sweep(args):
     """q_len-1 stress sweep: batch x context grid, one layer, default split;
     L2 flushed (a 256 MiB write) before every timed call so small points are
@@ -698,6 +719,8 @@ def run_sweep(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     drain = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB read after the flush
     free, _ = torch.cuda.mem_get_info(dev)
+    quant = args.kv in ("q8_0", "fp8_e4m3")
+    fp8 = args.kv == "fp8_e4m3"
     batches = [int(x) for x in args.sweep_batches.split(",")] if args.sweep_batches else W.SWEEP_BATCHES
     contexts = [int(x) for x in args.sweep_contexts.split(",")] if args.sweep_contexts else W.SWEEP_CONTEXTS
     peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("hbm_gbs", 6800.0) if os.path.exists(
@@ -711,17 +734,25 @@ def run_sweep(args):
                 points.append({"batch": b, "ctx": c, "skipped": "pool larger than free device memory"})
                 continue
             w = W.build(f"sweep", [c] * b, nb, seed=b * 7919 + c, fill_cache=False)
-            kc = torch.empty((nb, 8, 16, 128), dtype=torch.bfloat16, device=dev)
-            vc = torch.empty_like(kc)
-            W.fill_pool_device(kc, 2 * b + 1)
-            W.fill_pool_device(vc, 2 * b + 2)
+            if quant:  # N(0,1) values through the format's append, a chunk of blocks at a time
+                kc, vc = quantised_pools(pkv, args.kv, nb, 2 * b + 1, dev)
+            else:
+                kc = torch.empty((nb, 8, 16, 128), dtype=torch.bfloat16, device=dev)
+                vc = torch.empty_like(kc)
+                W.fill_pool_device(kc, 2 * b + 1)
+                W.fill_pool_device(vc, 2 * b + 2)
             q = torch.from_numpy(w.q).view(torch.bfloat16).to(dev)
             tables = torch.from_numpy(w.block_tables).to(dev)
             ctx = torch.from_numpy(w.context_lens).to(dev)
             out = torch.empty_like(q)
             maxb = w.max_blocks_per_seq
-            bps = pkv.choose_kv_blocks_per_split(b, 8, 1, maxb)
-            ws = torch.empty(max(256, pkv.workspace_size(b, 1, 32, maxb, bps)), dtype=torch.uint8, device=dev)
+            if quant:
+                choose = pkv.choose_kv_blocks_per_split_fp8_e4m3 if fp8 else pkv.choose_kv_blocks_per_split_q8_0
+                bps = choose(b, 8, maxb)
+                ws = torch.empty(max(256, pkv.workspace_size_q8_0(b, 32, maxb, bps)), dtype=torch.uint8, device=dev)
+            else:
+                bps = pkv.choose_kv_blocks_per_split(b, 8, 1, maxb)
+                ws = torch.empty(max(256, pkv.workspace_size(b, 1, 32, maxb, bps)), dtype=torch.uint8, device=dev)
             times = []
             for it in range(args.warmup + args.sweep_reps):
                 flush.fill_(it & 0xFF)
@@ -729,20 +760,26 @@ def run_sweep(args):
                 torch.cuda._sleep(200000)  # ~100 us: the call below is enqueued before the GPU reaches it
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                pkv.paged_attention(out, q, kc, vc, tables, ctx, 1, w.scale, kv_blocks_per_split=bps, workspace=ws)
+                if quant:
+                    (pkv.paged_attention_fp8_e4m3 if fp8 else pkv.paged_attention_q8_0)(
+                        out, q, kc, vc, tables, ctx, w.scale, kv_blocks_per_split=bps, workspace=ws)
+                else:
+                    pkv.paged_attention(out, q, kc, vc, tables, ctx, 1, w.scale, kv_blocks_per_split=bps,
+                                        workspace=ws)
                 e1.record(stream)
                 e1.synchronize()
                 if it >= args.warmup:
                     times.append(e0.elapsed_time(e1))
             us = statistics.median(times) * 1e3
-            attn_b, _ = bytes_per_layer(w)
+            attn_b, _ = bytes_per_layer(w, args.kv)
             points.append({"batch": b, "ctx": c, "us": round(us, 2), "gbs": round(attn_b / (us * 1e-6) / 1e9, 1),
                            "frac": round(attn_b / (us * 1e-6) / 1e9 / peak, 4), "splits": -(-maxb // bps)})
             del kc, vc, q, out, ws
             torch.cuda.empty_cache()
     if pkv.get_device_error(reset=True) != 0:
         raise RuntimeError("device error word set during the sweep")
-    print(json.dumps({"metric": "paged decode attention sweep (q_len 1, one layer, L2 flushed)", "peak_gbs": peak,
+    print(json.dumps({"metric": "paged decode attention sweep (q_len 1, one layer, L2 flushed)", "kv_format": args.kv,
+                      "peak_gbs": peak,
                       "reps": args.sweep_reps, "points": points}), flush=True)
 
 
