@@ -784,13 +784,18 @@ def run_sweep(args):
 
 
 def kernel_build_id() -> str:
-    """Hash of the CUDA sources: traffic numbers are valid only for the build they were taken on."""
+    """Hash of the CUDA sources' code (comments and blank space left out):
+    traffic numbers are valid only for the code they were taken on."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_attention_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, fn), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
         h.update(fn.encode())
-        h.update(open(os.path.join(csrc, fn), "rb").read())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -199,7 +199,6 @@ __device__ __forceinline__ bool merge_sync(uint64_t* merge, uint32_t& n, int lan
 // q8_0 tiles: int8 codes + FP16 group scales, 2176 B per (block, KV head).
 __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const DecodeArgs a) {
   constexpr int kTile = kQ8TileBytes;
-  pdl_wait();  // inputs may come from the previous grid (e.g. this step's append)
   pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem[];
   Q8Bars* bars = reinterpret_cast<Q8Bars*>(smem + kOffBarQ8);
@@ -236,6 +235,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  // The set-up above reads no input; everything below may read what earlier
+  // grids in the stream write (e.g. this step's append), so wait for them here.
+  pdl_wait();
   const uint32_t tmem = bars->tmem_base;
   const uint32_t sbase = smem_addr(smem);
   bool ok = true;
@@ -259,7 +261,12 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
       const Unit x = unit_at(a, u);
       const int32_t* table = a.block_tables + static_cast<int64_t>(x.r) * a.max_blocks;
-      auto entry = [&](int bi) -> int { return bi < x.b1 ? table[bi] : 0; };  // checked where used
+      // the load stays inside the table row whatever the context length, so it
+      // need not wait for that length; entries past the unit's blocks are dropped
+      auto entry = [&](int bi) -> int {
+        const int raw = table[min(bi, a.max_blocks - 1)];
+        return bi < x.b1 ? raw : 0;  // checked where used
+      };
       int cur = entry(x.b0 + lane);
       int nxt = 0;
       for (int j = 0; j < x.n_tiles; ++j, ++i) {

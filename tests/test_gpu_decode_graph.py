@@ -103,6 +103,7 @@ CASES = {
     "bf16": dict(fmt=0, ctx=[37, 300, 129, 16, 700, 1, 0, 2049], bps=0),
     "bf16_split_workspace": dict(fmt=0, ctx=[37, 300, 129, 16, 700, 1, 0, 2049], bps=5),
     "bf16_chunk": dict(fmt=0, ctx=[40, 300, 129, 16, 700, 17], bps=0, q_len=16),
+    "bf16_q_len_4": dict(fmt=0, ctx=[40, 300, 129, 16, 700, 17], bps=0, q_len=4),
     "cascade": dict(fmt=0, ctx=[130, 200, 129, 140, 300, 50, 77, 16], bps=0, prefix=8,
                     sharers=[True] * 5 + [False] * 3),
     "q8_0": dict(fmt=1, ctx=[37, 300, 129, 16, 700, 1, 0, 2049], bps=0),
