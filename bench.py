@@ -376,7 +376,7 @@ def main():
     # append + attention (+ the combine pass when splits go through the workspace: more than 8
     # splits, or any split on the tensor-core paths -- chunks, quantised pools and q_len-1 batches
     # of at least 2 (request, KV head) rows per SM)
-    tc_decode = ql == 1 and b * hkv >= 2 * torch.cuda.get_device_properties(dev).multi_processor_count
+    tc_decode = decode_on_tensor_cores(b, hkv, ql, maxb, torch.cuda.get_device_properties(dev).multi_processor_count)
     launches_per_layer = 1 + 1 + (1 if (splits > 8 or (splits > 1 and (ql >= 16 or q8 or tc_decode))) else 0)
     # shared prefixes: the caller states the groups and the cascade call reads each prefix once per group
     gs_h, gb_h, sp_h = W.prefix_groups(w)
@@ -449,6 +449,8 @@ def main():
             cascade={"num_groups": int(gs_h.shape[0]), "max_prefix_blocks": maxp, "max_suffix_blocks": maxs,
                      "prefix_blocks_per_split": pbps, "suffix_blocks_per_split": sbps} if cascade else None)
         run_step = lambda events=None: graph.launch(0, stream)
+        if not q8 and not cascade and ql == 1 and t_tok == b and not tc_decode:
+            launches_per_layer -= 1  # the graph's BF16 decode layers fuse the append into the attention kernel
     else:
         run_step = step
 
@@ -702,6 +704,23 @@ def quantised_pools(pkv, kv: str, nb: int, seed: int, dev, chunk: int = 4096):
         append(kq, vq, slots, tk[:n].permute(0, 2, 1, 3).contiguous().view(n * 16, 8, 128),
                tv[:n].permute(0, 2, 1, 3).contiguous().view(n * 16, 8, 128))
     return kq, vq
+
+
+def decode_on_tensor_cores(num_seqs: int, num_kv_heads: int, q_len: int, max_blocks: int, sms: int) -> bool:
+    """The library's choice of the persistent tensor-core decode (pkv_api.cu),
+    restated to count the step's launches: from 2 (request, KV head) rows per
+    SM, or from 3/4 of a row per SM with requests of >= 128 blocks when the
+    CTA-per-row kernel's one wave of 2 CTAs per SM would fill < 90 % of it."""
+    if q_len != 1:
+        return False
+    rows, slots = num_seqs * num_kv_heads, 2 * sms
+    if rows >= 2 * sms:
+        return True
+    if 4 * rows < 3 * sms or max_blocks < 128:
+        return False
+    splits = slots // rows
+    bps = max_blocks if (max_blocks <= 16 or splits <= 1) else min(max(16, -(-max_blocks // splits)), max_blocks)
+    return 10 * rows * (-(-max_blocks // bps)) < 9 * slots
 
 
 def run_sweep(args):

@@ -206,6 +206,33 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
                                        int32_t prefix_blocks_per_split, int32_t suffix_blocks_per_split,
                                        void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * pkv_paged_attention_append -- pkv_kv_append followed by pkv_paged_attention,
+ * in one call: the step's new tokens are stored (slot_mapping, k_new, v_new,
+ * num_tokens as for pkv_kv_append), then attention runs over the pools that
+ * hold them (every other argument as for pkv_paged_attention).  Ch8 §8.1.1:
+ * a decode step stores the new token's K and V and reads the context KV,
+ * the new token included.
+ *
+ * When q_len is 1, num_tokens == num_seqs and the decode runs on the
+ * CTA-per-row kernel (pkv_paged_attention's choice), both happen in one
+ * launch: the kernel block that reads the block holding request r's position
+ * context_lens[r] - 1 stores token r's K/V row there and uses it in place of
+ * the row it read.  That requires token r to be request r's new token and
+ * slot_mapping[r] to be the slot the block table gives that position (or
+ * negative: not stored); any other slot is stored as pkv_kv_append would but
+ * sets PKV_DEVERR_SLOT, and the attention result is then undefined.  Other
+ * shapes issue the append, then the attention.  Results equal the two calls'
+ * bit for bit.  Host-detectable errors of either call return before
+ * anything is enqueued.
+ */
+pkv_status pkv_paged_attention_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                      const pkv_cache_desc* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t q_len, int32_t num_q_heads, float scale, int32_t kv_blocks_per_split,
+                                      void* workspace, size_t workspace_bytes, const int64_t* slot_mapping,
+                                      const void* k_new, const void* v_new, int32_t num_tokens, void* stream);
+
 /* Bytes of the scratch array compiled into libpkv for
  * pkv_paged_attention_static_workspace (held on every GPU that loads the
  * library, until the process exits). */
@@ -469,8 +496,9 @@ const char* pkv_status_string(pkv_status status);
  *   workspace          : the attention call's workspace (the graphs run in
  *                        stream order, so one serves both), sized by
  *                        pkv_workspace_size / _q8_0 / pkv_cascade_workspace_size
- * kv_format: PKV_KV_BF16 (pkv_kv_append + pkv_paged_attention, or
- * pkv_paged_attention_cascade when num_groups > 0), PKV_KV_Q8_0 or
+ * kv_format: PKV_KV_BF16 (pkv_paged_attention_append -- one launch per layer
+ * where it fuses the two -- or pkv_kv_append + pkv_paged_attention_cascade
+ * when num_groups > 0), PKV_KV_Q8_0 or
  * PKV_KV_FP8_E4M3 (their append and decode calls; q_len 1, no groups).
  * Split sizes as for the direct calls (0 = the library's heuristic).
  *

@@ -202,6 +202,18 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
   const int b1 = min(nb, b0 + a.blocks_per_split);
   const int64_t qrow0 = static_cast<int64_t>(vrow) * hq + kvh * kGroup;  // (r, i, first head of group)
   const bool empty = b0 >= b1;
+  // Fused append (q_len 1): the iteration of this CTA whose block holds the
+  // new token (position ctx - 1), or -1 when another CTA holds it or the
+  // token is not stored.
+  int new_it = -1;
+  int64_t new_slot = -1;
+  if (a.k_new != nullptr && ctx > 0 && ctx <= a.max_blocks * kBlockSize) {
+    const int nbl = (ctx - 1) / kBlockSize;
+    if (nbl >= b0 && nbl < b1) {
+      new_slot = a.slot_mapping[r];
+      if (new_slot >= 0) new_it = nbl - b0;
+    }
+  }
 
   const bool has_prefix = a.prefix_o != nullptr && start > 0;
   if (empty) {  // nothing to read: padding row, query without keys, or a split past the context
@@ -336,11 +348,43 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
       const int tk1 = tk0 + 4;
       bool ok = true;
 
+      // Fused append: the warp that reduces the new token's block stores the
+      // token's K/V row (8 bytes per lane) into the pools, where the append
+      // would, and patches it into the block's tile once that has landed --
+      // the copy may have read the slot before or after the store.
+      bool patch = false;
+      int new_off = 0;
+      uint2 kn8 = make_uint2(0, 0), vn8 = make_uint2(0, 0);
+      if (new_it >= 0 && new_it % kConsumerWarps == warp) {
+        new_off = (ctx - 1) % kBlockSize;
+        const int pb = a.block_tables[static_cast<int64_t>(r) * a.max_blocks + b0 + new_it];
+        const int64_t row = static_cast<int64_t>(r) * a.num_kv_heads + kvh;  // token r, KV head kvh
+        kn8 = reinterpret_cast<const uint2*>(a.k_new)[row * (kRowBytes / 8) + lane];
+        vn8 = reinterpret_cast<const uint2*>(a.v_new)[row * (kRowBytes / 8) + lane];
+        const int64_t pool_slots = static_cast<int64_t>(a.num_blocks) * kBlockSize;
+        if (new_slot < pool_slots) {
+          const size_t off = (static_cast<size_t>(new_slot / kBlockSize) * a.num_kv_heads + kvh) * kTileBytes +
+                             static_cast<size_t>(new_slot % kBlockSize) * kRowBytes + lane * 8;
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(const_cast<void*>(a.k_cache)) + off) = kn8;
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(const_cast<void*>(a.v_cache)) + off) = vn8;
+        }
+        // the slot must be the one the table gives position ctx - 1
+        patch = new_slot == static_cast<int64_t>(pb) * kBlockSize + new_off;
+        if (!patch && lane == 0) report(a.err, PKV_DEVERR_SLOT);
+      }
+
       for (int it = warp; it < n_iter; it += kConsumerWarps) {
         const int st = it % NS;
         if (!mbar_wait(&full_bar[st], (it / NS) & 1)) {
           ok = false;
           break;
+        }
+        if (patch && it == new_it) {
+          uint8_t* kw = stages + st * kStageBytes + new_off * kRowBytes + lane * 8;
+          *reinterpret_cast<uint2*>(kw) = kn8;
+          *reinterpret_cast<uint2*>(kw + kTileBytes) = vn8;
+          fence_proxy_async_shared();  // the stage is refilled by a bulk copy later
+          __syncwarp();
         }
         const uint8_t* ks = stages + st * kStageBytes;
         const uint8_t* vs = ks + kTileBytes;

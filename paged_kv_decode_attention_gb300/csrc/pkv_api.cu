@@ -208,11 +208,24 @@ size_t pkv_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads, 
   return align_up(rows * splits * head_dim * sizeof(float), 256) + align_up(rows * splits * sizeof(float), 256);
 }
 
-pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
-                               const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
-                               const int32_t* context_lens, int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
-                               float scale, int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
-                               void* stream) {
+}  // extern "C"
+
+namespace {
+
+// pkv_paged_attention's checks and launches.  fused (optional): the append
+// fused into the CTA-per-row decode kernel (q_len 1; the caller has checked
+// that this kernel runs).  dry_run: every check, no launch.
+struct FusedAppend {
+  const int64_t* slot_mapping;
+  const void* k_new;
+  const void* v_new;
+};
+
+pkv_status paged_attention_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                float scale, int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
+                                void* stream, const FusedAppend* fused, bool dry_run) {
   pkv_status st = check_cache(cache);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || q_len < 1 || max_blocks_per_seq < 1 || kv_blocks_per_split < 0) return PKV_ERR_SHAPE;
@@ -250,6 +263,11 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
   a.scale_log2 = scale * 1.4426950408889634f;
   a.part_slots = splits;
   a.part_slot0 = 0;
+  if (fused != nullptr) {
+    a.slot_mapping = fused->slot_mapping;
+    a.k_new = fused->k_new;
+    a.v_new = fused->v_new;
+  }
   const int32_t tc_grid_x = num_seqs * ((q_len + 15) / 16);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -258,10 +276,14 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
     const int64_t units = static_cast<int64_t>(num_seqs) * cache->num_kv_heads * splits;
     if (units > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     const int32_t grid = static_cast<int32_t>(units < sms ? units : sms);
-    if (splits == 1) return launch_paged_decode_tc(a, grid, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    if (splits == 1) {
+      if (dry_run) return PKV_OK;
+      return launch_paged_decode_tc(a, grid, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    }
     const size_t need = pkv_workspace_size(num_seqs, 1, num_q_heads, kHeadDim, max_blocks_per_seq, bps);
     if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+    if (dry_run) return PKV_OK;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
     a.part_o = static_cast<float*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
@@ -277,6 +299,7 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
     const size_t need = pkv_workspace_size(num_seqs, q_len, num_q_heads, kHeadDim, max_blocks_per_seq, bps);
     if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+    if (dry_run) return PKV_OK;
     const size_t rows = static_cast<size_t>(num_seqs) * q_len * num_q_heads;
     a.part_o = static_cast<float*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
@@ -287,8 +310,60 @@ pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, co
       return PKV_ERR_CUDA;
     return PKV_OK;
   }
+  if (dry_run) return PKV_OK;
   return (tensor_cores ? launch_paged_chunk_tc(a, tc_grid_x, s) : launch_paged_decode(a, s)) == cudaSuccess ? PKV_OK
                                                                                                  : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                               float scale, int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  return paged_attention_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                              num_seqs, q_len, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes,
+                              stream, nullptr, false);
+}
+
+pkv_status pkv_paged_attention_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                      const pkv_cache_desc* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t q_len, int32_t num_q_heads, float scale, int32_t kv_blocks_per_split,
+                                      void* workspace, size_t workspace_bytes, const int64_t* slot_mapping,
+                                      const void* k_new, const void* v_new, int32_t num_tokens, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens > 0) {
+    if (!k_cache || !v_cache || !slot_mapping || !k_new || !v_new) return PKV_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return PKV_ERR_UNSUPPORTED;
+  }
+  // every check of the attention first, so an error enqueues nothing
+  st = paged_attention_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                            num_seqs, q_len, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes,
+                            stream, nullptr, true);
+  if (st != PKV_OK) return st;
+  // one launch when each request appends its one new token and the decode
+  // runs on the CTA-per-row kernel; otherwise the append, then the attention
+  const bool fuse = q_len == 1 && num_tokens == num_seqs && num_seqs > 0 &&
+                    !decode_on_tensor_cores(num_seqs, cache->num_kv_heads, 1, max_blocks_per_seq, device_sm_count());
+  if (fuse) {
+    const FusedAppend f{slot_mapping, k_new, v_new};
+    return paged_attention_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                                num_seqs, q_len, num_q_heads, scale, kv_blocks_per_split, workspace,
+                                workspace_bytes, stream, &f, false);
+  }
+  if (num_tokens > 0) {
+    st = pkv_kv_append(k_cache, v_cache, cache, slot_mapping, k_new, v_new, num_tokens, stream);
+    if (st != PKV_OK) return st;
+  }
+  return paged_attention_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                              num_seqs, q_len, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes,
+                              stream, nullptr, false);
 }
 
 void pkv_cascade_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_groups, int32_t max_prefix_blocks,

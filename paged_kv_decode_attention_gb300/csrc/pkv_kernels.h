@@ -88,6 +88,15 @@ struct DecodeArgs {
   // complete before that pass started, so it starts at once (overlapping the
   // pass) and waits for the pass only before it exits.
   int32_t overlap_previous;
+  // Append fused into the decode kernel (q_len 1, CTA-per-row kernel): token
+  // r of k_new/v_new ([num_seqs][Hkv][128] BF16) is request r's new token, at
+  // position context_lens[r] - 1, stored at slot_mapping[r] (< 0 = not
+  // stored).  The CTA whose block range holds that position writes the row
+  // into the pools and uses it in place of the tile's stale row.  NULL = no
+  // append.
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
 };
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,

@@ -1,0 +1,128 @@
+"""pkv_paged_attention_append: the append and the attention of a decode step
+in one call.  Where it fuses them into one kernel (q_len 1 on the CTA-per-row
+decode kernel) and where it issues the two launches, its output and the pools
+it leaves must equal pkv_kv_append followed by pkv_paged_attention bit for
+bit; the result must also match the FP64 oracle; and a slot that is not the
+one the block table gives the new token's position sets the device error
+word."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_util import assert_close, bf16_to_f64, to_device
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import paged_kv_decode_attention_gb300 as pkv
+else:  # collected on CPU-only machines, every test skipped
+    pkv = None
+
+
+@pytest.fixture(autouse=True)
+def _clear_device_error():
+    if pkv is not None:
+        pkv.get_device_error(reset=True)
+    yield
+    if pkv is not None:
+        assert pkv.get_device_error(reset=True) == 0
+
+
+def _both(w, bps=0, d=None):
+    """(fused call, separate calls) on copies of the same device state: outputs and pools."""
+    if d is None:
+        d = to_device(w)
+    maxb = w.max_blocks_per_seq
+    if bps == 0:
+        bps = pkv.choose_kv_blocks_per_split(w.num_seqs, w.num_kv_heads, w.q_len, maxb)
+    ws = torch.empty(max(pkv.workspace_size(w.num_seqs, w.q_len, w.num_q_heads, maxb, bps), 256), dtype=torch.uint8,
+                     device="cuda")
+    res = []
+    for fused in (True, False):
+        kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+        out = torch.full_like(d["q"], float("nan"))
+        if fused:
+            pkv.paged_attention_append(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.q_len, w.scale,
+                                       d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=bps,
+                                       workspace=ws)
+        else:
+            pkv.kv_append(kc, vc, d["slot_mapping"], d["k_new"], d["v_new"])
+            pkv.paged_attention(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.q_len, w.scale,
+                                kv_blocks_per_split=bps, workspace=ws)
+        torch.cuda.synchronize()
+        res.append((out, kc, vc))
+    return res
+
+
+def _assert_same(res, what):
+    (of, kf, vf), (os_, ks, vs) = res
+    assert torch.equal(of.view(torch.int16), os_.view(torch.int16)), f"{what}: outputs differ"
+    assert torch.equal(kf.view(torch.int16), ks.view(torch.int16)), f"{what}: K pools differ"
+    assert torch.equal(vf.view(torch.int16), vs.view(torch.int16)), f"{what}: V pools differ"
+
+
+# contexts that put the new token at a block's first slot (17, 2049), last slot (16, 32) or
+# alone (1), and a padding row (0, slot -1)
+RAGGED = [17, 300, 1, 16, 700, 0, 32, 2049, 129, 55]
+
+
+@pytest.mark.parametrize("bps", [0, 1000, 5, 24])
+def test_fused_decode_equals_append_then_attention(bps):
+    """One kernel on the CTA-per-row decode: no split (1000), cluster-merged
+    splits (0, 24) and workspace splits merged by the combine kernel (5)."""
+    ctx = np.asarray(RAGGED)
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("fused", ctx, need + 30, seed=61)
+    res = _both(w, bps)
+    _assert_same(res, f"fused bps={bps}")
+    assert not res[0][0][ctx == 0].float().abs().sum()
+    assert_close(bf16_to_f64(res[0][0]), oracle.run_workload(w), what=f"fused vs oracle bps={bps}")
+
+
+@pytest.mark.parametrize("num_seqs,q_len", [(24, 1), (6, 4), (5, 16)])
+def test_shapes_that_issue_two_launches(num_seqs, q_len):
+    """Tensor-core decode (24 requests of ~2K tokens), a 4-position query and
+    a 16-position chunk: the append, then the attention; same results."""
+    rng = np.random.default_rng(num_seqs + q_len)
+    ctx = rng.integers(1900 if q_len == 1 else q_len, 2300, size=num_seqs)
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("two-launch", ctx, need + 30, q_len=q_len, seed=62)
+    res = _both(w)
+    _assert_same(res, f"two launches {num_seqs}x{q_len}")
+    assert_close(bf16_to_f64(res[0][0]), oracle.run_workload(w), what=f"two launches {num_seqs}x{q_len}")
+
+
+def test_unstored_token_reads_the_pool_as_it_is():
+    """A request whose new token is not stored (slot -1) attends over the pool
+    as it stands, as the separate calls do."""
+    ctx = np.asarray(RAGGED)
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("unstored", ctx, need + 30, seed=63)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[[1, 7]] = -1
+    _assert_same(_both(w), "unstored token")
+
+
+def test_slot_other_than_the_tables_sets_the_error_word():
+    ctx = np.asarray([100, 200, 300])
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("bad-slot", ctx, need + 30, seed=64)
+    used = set()
+    for r, c in enumerate(ctx):
+        used.update(int(b) for b in w.block_tables[r, :-(-int(c) // 16)])
+    spare = next(b for b in range(w.num_blocks) if b not in used)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[1] = spare * 16 + 3  # stored there, but not at request 1's position
+    d = to_device(w)
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(d["q"])
+    pkv.paged_attention_append(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], 1,
+                               w.scale, d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=1000,
+                               workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(reset=True) == pkv.DEVERR_SLOT
+    # the token is stored where the slot says, as the append would
+    kc = d["k_cache"].view(torch.int16).cpu().numpy()
+    assert np.array_equal(kc[spare, :, 3, :], w.k_new.view(np.int16)[1])
