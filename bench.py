@@ -449,7 +449,7 @@ def main():
             cascade={"num_groups": int(gs_h.shape[0]), "max_prefix_blocks": maxp, "max_suffix_blocks": maxs,
                      "prefix_blocks_per_split": pbps, "suffix_blocks_per_split": sbps} if cascade else None)
         run_step = lambda events=None: graph.launch(0, stream)
-        if not q8 and not cascade and ql == 1 and t_tok == b and not tc_decode:
+        if not q8 and ql == 1 and t_tok == b and (cascade or not tc_decode):
             launches_per_layer -= 1  # the graph's BF16 decode layers fuse the append into the attention kernel
     else:
         run_step = step

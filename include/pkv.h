@@ -233,6 +233,24 @@ pkv_status pkv_paged_attention_append(void* out, const void* q, void* k_cache, v
                                       void* workspace, size_t workspace_bytes, const int64_t* slot_mapping,
                                       const void* k_new, const void* v_new, int32_t num_tokens, void* stream);
 
+/*
+ * pkv_paged_attention_cascade_append -- pkv_kv_append followed by
+ * pkv_paged_attention_cascade, in one call (arguments as for the two).  When
+ * num_tokens == num_seqs (token r is request r's new token) the suffix pass
+ * stores the tokens and uses them as pkv_paged_attention_append's single
+ * launch does; other counts issue the append, then the cascade.  A new token
+ * must lie past its request's shared prefix (never append into a block
+ * another table references); one inside it is not stored and sets
+ * PKV_DEVERR_SLOT.  Results equal the two calls' bit for bit otherwise.
+ */
+pkv_status pkv_paged_attention_cascade_append(
+    void* out, const void* q, void* k_cache, void* v_cache, const pkv_cache_desc* cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
+    const int32_t* group_seqs, const int32_t* group_blocks, const int32_t* seq_prefix_blocks, int32_t num_groups,
+    int32_t max_prefix_blocks, int32_t max_suffix_blocks, int32_t prefix_blocks_per_split,
+    int32_t suffix_blocks_per_split, void* workspace, size_t workspace_bytes, const int64_t* slot_mapping,
+    const void* k_new, const void* v_new, int32_t num_tokens, void* stream);
+
 /* Bytes of the scratch array compiled into libpkv for
  * pkv_paged_attention_static_workspace (held on every GPU that loads the
  * library, until the process exits). */
@@ -496,9 +514,9 @@ const char* pkv_status_string(pkv_status status);
  *   workspace          : the attention call's workspace (the graphs run in
  *                        stream order, so one serves both), sized by
  *                        pkv_workspace_size / _q8_0 / pkv_cascade_workspace_size
- * kv_format: PKV_KV_BF16 (pkv_paged_attention_append -- one launch per layer
- * where it fuses the two -- or pkv_kv_append + pkv_paged_attention_cascade
- * when num_groups > 0), PKV_KV_Q8_0 or
+ * kv_format: PKV_KV_BF16 (pkv_paged_attention_append, or
+ * pkv_paged_attention_cascade_append when num_groups > 0: the append fused
+ * into the attention where they can), PKV_KV_Q8_0 or
  * PKV_KV_FP8_E4M3 (their append and decode calls; q_len 1, no groups).
  * Split sizes as for the direct calls (0 = the library's heuristic).
  *

@@ -21,7 +21,7 @@ from . import build as _build
 
 __all__ = [
     "PkvError", "BlockPool", "copy_blocks", "kv_append", "paged_attention", "paged_attention_append",
-    "paged_attention_cascade", "cascade_plan",
+    "paged_attention_cascade", "paged_attention_cascade_append", "cascade_plan",
     "cascade_workspace_size", "attn_combine", "workspace_size",
     "choose_kv_blocks_per_split", "get_device_error", "library_path", "lib", "DEVERR_BLOCK_ID",
     "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "Q8_TILE_BYTES", "kv_append_q8_0", "paged_attention_q8_0",
@@ -135,6 +135,9 @@ def _load():
     lib.pkv_paged_attention_append.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32, i32, f32,
                                                i32, p, sz, p, p, p, i32, p]
     lib.pkv_paged_attention_append.restype = ctypes.c_int
+    lib.pkv_paged_attention_cascade_append.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32,
+                                                       f32, p, p, p, i32, i32, i32, i32, i32, p, sz, p, p, p, i32, p]
+    lib.pkv_paged_attention_cascade_append.restype = ctypes.c_int
     lib.pkv_decode_graph_create.argtypes = [ctypes.POINTER(DecodeGraphDesc), ctypes.POINTER(ctypes.c_void_p)]
     lib.pkv_decode_graph_create.restype = ctypes.c_int
     lib.pkv_decode_graph_launch.argtypes = [p, i32, p]
@@ -326,6 +329,40 @@ def paged_attention_cascade(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
         group_seqs.data_ptr() if g else 0, group_blocks.data_ptr() if g else 0, seq_prefix_blocks.data_ptr(), g,
         int(max_prefix_blocks), int(max_suffix_blocks), int(prefix_blocks_per_split), int(suffix_blocks_per_split),
         ws_ptr, ws_bytes, _stream_ptr(stream)), "pkv_paged_attention_cascade")
+
+
+def paged_attention_cascade_append(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                   scale: float, group_seqs: torch.Tensor, group_blocks: torch.Tensor,
+                                   seq_prefix_blocks: torch.Tensor, max_prefix_blocks: int, max_suffix_blocks: int,
+                                   workspace: torch.Tensor, slot_mapping: torch.Tensor, k_new: torch.Tensor,
+                                   v_new: torch.Tensor, prefix_blocks_per_split: int = 0,
+                                   suffix_blocks_per_split: int = 0, stream=None) -> None:
+    """kv_append, then paged_attention_cascade, as one call (the suffix pass stores the new tokens)."""
+    _bf16(out, "out"), _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    _bf16(k_new, "k_new"), _bf16(v_new, "v_new")
+    for t, n in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                 (seq_prefix_blocks, "seq_prefix_blocks")):
+        _i32(t, n)
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous CUDA int64 tensor")
+    b = context_lens.numel()
+    if q.dim() != 4 or q.shape[0] != b or q.shape[1] != 1 or out.shape != q.shape:
+        raise ValueError("q/out must be [num_seqs][1][num_q_heads][head_dim]")
+    g = group_seqs.shape[0] if group_seqs is not None else 0
+    if g:
+        _i32(group_seqs, "group_seqs"), _i32(group_blocks, "group_blocks")
+    desc = _desc(k_cache)
+    t = slot_mapping.numel()
+    if tuple(k_new.shape) != (t, desc.num_kv_heads, HEAD_DIM) or tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
+    _check(_lib.pkv_paged_attention_cascade_append(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), b, q.shape[2], float(scale),
+        group_seqs.data_ptr() if g else 0, group_blocks.data_ptr() if g else 0, seq_prefix_blocks.data_ptr(), g,
+        int(max_prefix_blocks), int(max_suffix_blocks), int(prefix_blocks_per_split), int(suffix_blocks_per_split),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), slot_mapping.data_ptr(),
+        k_new.data_ptr(), v_new.data_ptr(), t, _stream_ptr(stream)), "pkv_paged_attention_cascade_append")
 
 
 def attn_combine(out: torch.Tensor, partial_o: torch.Tensor, partial_lse: torch.Tensor,

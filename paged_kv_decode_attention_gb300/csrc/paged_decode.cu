@@ -212,6 +212,10 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
     if (nbl >= b0 && nbl < b1) {
       new_slot = a.slot_mapping[r];
       if (new_slot >= 0) new_it = nbl - b0;
+    } else if (nbl < start && split == 0 && kvh == 0 && threadIdx.x == 0 && a.slot_mapping[r] >= 0) {
+      // a new token inside a shared prefix (cascade): appending into a block
+      // other requests read is not allowed; it is not stored
+      report(a.err, PKV_DEVERR_SLOT);
     }
   }
 

@@ -408,14 +408,19 @@ size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t
   return align_up(rows * slots * kHeadDim * sizeof(float), 256) + align_up(rows * slots * sizeof(float), 256);
 }
 
-pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
-                                       const pkv_cache_desc* cache, const int32_t* block_tables,
-                                       int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
-                                       int32_t num_q_heads, float scale, const int32_t* group_seqs,
-                                       const int32_t* group_blocks, const int32_t* seq_prefix_blocks,
-                                       int32_t num_groups, int32_t max_prefix_blocks, int32_t max_suffix_blocks,
-                                       int32_t prefix_blocks_per_split, int32_t suffix_blocks_per_split,
-                                       void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// pkv_paged_attention_cascade's checks and launches; fused and dry_run as for
+// paged_attention_impl (the suffix pass always runs on the CTA-per-row kernel).
+pkv_status cascade_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
+                        const int32_t* group_seqs, const int32_t* group_blocks, const int32_t* seq_prefix_blocks,
+                        int32_t num_groups, int32_t max_prefix_blocks, int32_t max_suffix_blocks,
+                        int32_t prefix_blocks_per_split, int32_t suffix_blocks_per_split, void* workspace,
+                        size_t workspace_bytes, void* stream, const FusedAppend* fused, bool dry_run) {
   pkv_status st = check_cache(cache);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_blocks_per_seq < 1 || num_groups < 0 || max_prefix_blocks < 0 ||
@@ -469,6 +474,7 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
   a.part_o = part_o;
   a.part_lse = part_lse;
   a.part_slots = slots;
+  if (dry_run) return PKV_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (sp > 0) {
     // shared prefixes: each group's members x 4 heads as one 64-row tensor-core tile
@@ -485,6 +491,11 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
   a.num_splits = ss;
   a.seq_start_block = seq_prefix_blocks;
   a.overlap_previous = sp > 0 ? 1 : 0;  // the suffix pass runs beside the prefix pass
+  if (fused != nullptr) {  // the new tokens lie in the suffixes: the suffix pass stores them
+    a.slot_mapping = fused->slot_mapping;
+    a.k_new = fused->k_new;
+    a.v_new = fused->v_new;
+  }
   if (on_chip) {
     // direct (one split) or cluster merge, folding in the prefix partials: no combine kernel
     a.part_o = nullptr;
@@ -503,6 +514,61 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
   if (launch_attn_combine(out, nullptr, a.part_o, a.part_lse, static_cast<int32_t>(rows), slots, s) != cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const pkv_cache_desc* cache, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                       int32_t num_q_heads, float scale, const int32_t* group_seqs,
+                                       const int32_t* group_blocks, const int32_t* seq_prefix_blocks,
+                                       int32_t num_groups, int32_t max_prefix_blocks, int32_t max_suffix_blocks,
+                                       int32_t prefix_blocks_per_split, int32_t suffix_blocks_per_split,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  return cascade_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                      num_q_heads, scale, group_seqs, group_blocks, seq_prefix_blocks, num_groups, max_prefix_blocks,
+                      max_suffix_blocks, prefix_blocks_per_split, suffix_blocks_per_split, workspace,
+                      workspace_bytes, stream, nullptr, false);
+}
+
+pkv_status pkv_paged_attention_cascade_append(
+    void* out, const void* q, void* k_cache, void* v_cache, const pkv_cache_desc* cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
+    const int32_t* group_seqs, const int32_t* group_blocks, const int32_t* seq_prefix_blocks, int32_t num_groups,
+    int32_t max_prefix_blocks, int32_t max_suffix_blocks, int32_t prefix_blocks_per_split,
+    int32_t suffix_blocks_per_split, void* workspace, size_t workspace_bytes, const int64_t* slot_mapping,
+    const void* k_new, const void* v_new, int32_t num_tokens, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens > 0) {
+    if (!k_cache || !v_cache || !slot_mapping || !k_new || !v_new) return PKV_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return PKV_ERR_UNSUPPORTED;
+  }
+  // every check of the attention first, so an error enqueues nothing
+  st = cascade_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                    num_q_heads, scale, group_seqs, group_blocks, seq_prefix_blocks, num_groups, max_prefix_blocks,
+                    max_suffix_blocks, prefix_blocks_per_split, suffix_blocks_per_split, workspace, workspace_bytes,
+                    stream, nullptr, true);
+  if (st != PKV_OK) return st;
+  if (num_tokens == num_seqs && num_seqs > 0) {
+    const FusedAppend f{slot_mapping, k_new, v_new};
+    return cascade_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                        num_q_heads, scale, group_seqs, group_blocks, seq_prefix_blocks, num_groups,
+                        max_prefix_blocks, max_suffix_blocks, prefix_blocks_per_split, suffix_blocks_per_split,
+                        workspace, workspace_bytes, stream, &f, false);
+  }
+  if (num_tokens > 0) {
+    st = pkv_kv_append(k_cache, v_cache, cache, slot_mapping, k_new, v_new, num_tokens, stream);
+    if (st != PKV_OK) return st;
+  }
+  return cascade_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                      num_q_heads, scale, group_seqs, group_blocks, seq_prefix_blocks, num_groups, max_prefix_blocks,
+                      max_suffix_blocks, prefix_blocks_per_split, suffix_blocks_per_split, workspace,
+                      workspace_bytes, stream, nullptr, false);
 }
 
 pkv_status pkv_kv_append_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc* cache,

@@ -126,3 +126,64 @@ def test_slot_other_than_the_tables_sets_the_error_word():
     # the token is stored where the slot says, as the append would
     kc = d["k_cache"].view(torch.int16).cpu().numpy()
     assert np.array_equal(kc[spare, :, 3, :], w.k_new.view(np.int16)[1])
+
+
+def _cascade_both(w, pbps, sbps):
+    gs, gb, sp = W.prefix_groups(w)
+    maxp, maxs = int(gb.max()), W.max_suffix_blocks(w, sp)
+    b, hq = w.num_seqs, w.num_q_heads
+    pb, sb = pkv.cascade_plan(b, w.num_kv_heads, gs.shape[0], maxp, maxs)
+    pb, sb = pbps or pb, sbps or sb
+    ws = torch.empty(max(256, pkv.cascade_workspace_size(b, hq, maxp, maxs, pb, sb)), dtype=torch.uint8,
+                     device="cuda")
+    d = to_device(w)
+    gs_d, gb_d, sp_d = (torch.from_numpy(x).cuda() for x in (gs, gb, sp))
+    res = []
+    for fused in (True, False):
+        kc, vc = d["k_cache"].clone(), d["v_cache"].clone()
+        out = torch.full_like(d["q"], float("nan"))
+        if fused:
+            pkv.paged_attention_cascade_append(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
+                                               gs_d, gb_d, sp_d, maxp, maxs, ws, d["slot_mapping"], d["k_new"],
+                                               d["v_new"], pb, sb)
+        else:
+            pkv.kv_append(kc, vc, d["slot_mapping"], d["k_new"], d["v_new"])
+            pkv.paged_attention_cascade(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale, gs_d,
+                                        gb_d, sp_d, maxp, maxs, ws, pb, sb)
+        torch.cuda.synchronize()
+        res.append((out, kc, vc))
+    return res
+
+
+@pytest.mark.parametrize("pbps,sbps", [(0, 0), (4, 3), (16, 2)])
+def test_fused_cascade_equals_append_then_cascade(pbps, sbps):
+    """Five sharers of an 8-block prefix and three requests outside it; suffix
+    splits merged in a cluster (0, 3) or through the workspace (2)."""
+    ctx = [130, 200, 129, 140, 300, 50, 77, 16]
+    w = W.build("casc-fused", ctx, 120, seed=65, shared_prefix_blocks=8, sharers=[True] * 5 + [False] * 3)
+    res = _cascade_both(w, pbps, sbps)
+    _assert_same(res, f"fused cascade pbps={pbps} sbps={sbps}")
+    assert_close(bf16_to_f64(res[0][0]), oracle.run_workload(w), what=f"fused cascade pbps={pbps} sbps={sbps}")
+
+
+def test_fused_cascade_token_inside_the_shared_prefix_sets_the_error_word():
+    ctx = [130, 200, 129, 140, 300, 50]
+    w = W.build("casc-inside", ctx, 120, seed=66, shared_prefix_blocks=8, sharers=[True] * 5 + [False])
+    gs, gb, sp = W.prefix_groups(w)
+    # request 0 now ends inside the 8-block prefix: its new token (position 99) would go to a shared block
+    w.context_lens = w.context_lens.copy()
+    w.context_lens[0] = 100
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[0] = int(w.block_tables[0, 99 // 16]) * 16 + 99 % 16
+    maxp, maxs = int(gb.max()), W.max_suffix_blocks(w, sp)
+    ws = torch.empty(max(256, pkv.cascade_workspace_size(w.num_seqs, w.num_q_heads, maxp, maxs,
+                                                         *pkv.cascade_plan(w.num_seqs, w.num_kv_heads, gs.shape[0],
+                                                                           maxp, maxs))), dtype=torch.uint8,
+                     device="cuda")
+    d = to_device(w)
+    out = torch.empty_like(d["q"])
+    pkv.paged_attention_cascade_append(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                       d["context_lens"], w.scale, *(torch.from_numpy(x).cuda() for x in (gs, gb, sp)),
+                                       maxp, maxs, ws, d["slot_mapping"], d["k_new"], d["v_new"])
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(reset=True) == pkv.DEVERR_SLOT
