@@ -187,3 +187,19 @@ def test_fused_cascade_token_inside_the_shared_prefix_sets_the_error_word():
                                        maxp, maxs, ws, d["slot_mapping"], d["k_new"], d["v_new"])
     torch.cuda.synchronize()
     assert pkv.get_device_error(reset=True) == pkv.DEVERR_SLOT
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fused_random_shapes(seed):
+    """Seeded random batches (1-60 requests, 0-3000 tokens, some tokens not
+    stored, any split): every dispatch path, bit-equal to the separate calls."""
+    rng = np.random.default_rng(1000 + seed)
+    b = int(rng.integers(1, 61))
+    ctx = rng.integers(0, 3001, size=b)
+    ctx[rng.random(b) < 0.1] = 0
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("fused-rand", ctx, need + 16, seed=2000 + seed)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[rng.random(b) < 0.1] = -1
+    bps = int(rng.choice([0, 0, 3, 16, 40, 1000]))
+    _assert_same(_both(w, bps), f"random seed={seed} b={b} bps={bps}")
