@@ -845,7 +845,11 @@ def run_reference(args, world, rank, w, layers, step_bytes):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_seqs": w.num_seqs,
+                       "q_len": w.q_len, "layers": layers, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                       "head_dim": w.head_dim, "block_size": 16, "ctx_min": int(w.context_lens.min()),
+                       "ctx_max": int(w.context_lens.max()), "kv_format": args.kv,
+                       "parallelism": f"replicas x{world}"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
                              "cores": oracle.max_threads(), "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
