@@ -96,8 +96,8 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else f"/tmp/pkv_clocks_{os.getpid()}.csv"
+        # PKV_CLOCKS_CSV keeps the raw samples where the caller wants them
+        self.path = os.environ.get("PKV_CLOCKS_CSV") or f"/tmp/pkv_clocks_{gpu_index}_{os.getpid()}.csv"
         self.gpu = gpu_index
 
     def start(self):
