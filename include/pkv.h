@@ -473,6 +473,25 @@ pkv_status pkv_paged_attention_fp8_e4m3(void* out, const void* q, const void* k_
                                         int32_t num_q_heads, float scale, int32_t kv_blocks_per_split,
                                         void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * pkv_paged_attention_fp8_e4m3_append -- pkv_kv_append_fp8_e4m3 followed by
+ * pkv_paged_attention_fp8_e4m3, in one call (arguments as for the two).  When
+ * num_tokens == num_seqs (token r is request r's new token, at position
+ * context_lens[r] - 1) the decode kernel rounds and stores the tokens itself
+ * and uses them in place of the rows it read, as pkv_paged_attention_append
+ * does; other counts issue the append, then the attention.  A slot other than
+ * the one the block table gives that position is stored as the append would
+ * but sets PKV_DEVERR_SLOT (the result is then undefined).  Results equal the
+ * two calls' bit for bit otherwise.
+ */
+pkv_status pkv_paged_attention_fp8_e4m3_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                               const pkv_cache_desc* cache, const int32_t* block_tables,
+                                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                               int32_t num_seqs, int32_t num_q_heads, float scale,
+                                               int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
+                                               const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                                               int32_t num_tokens, void* stream);
+
 /* pkv_copy_blocks for E4M3 pools (num_kv_heads * PKV_FP8_TILE_BYTES per block). */
 pkv_status pkv_copy_blocks_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
                                     const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
@@ -515,9 +534,10 @@ const char* pkv_status_string(pkv_status status);
  *                        stream order, so one serves both), sized by
  *                        pkv_workspace_size / _q8_0 / pkv_cascade_workspace_size
  * kv_format: PKV_KV_BF16 (pkv_paged_attention_append, or
- * pkv_paged_attention_cascade_append when num_groups > 0: the append fused
- * into the attention where they can), PKV_KV_Q8_0 or
- * PKV_KV_FP8_E4M3 (their append and decode calls; q_len 1, no groups).
+ * pkv_paged_attention_cascade_append when num_groups > 0), PKV_KV_FP8_E4M3
+ * (pkv_paged_attention_fp8_e4m3_append) -- the append fused into the
+ * attention where they can -- or PKV_KV_Q8_0 (its append and decode calls);
+ * quantised pools: q_len 1, no groups.
  * Split sizes as for the direct calls (0 = the library's heuristic).
  *
  * Ownership and errors: create validates every call of the step with the

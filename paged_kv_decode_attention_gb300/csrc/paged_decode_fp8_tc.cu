@@ -76,7 +76,9 @@ constexpr int kOffV = kOffK + kFtStages * kFtStageBytes;
 constexpr int kOffQp = kOffV + kFtStages * kFtStageBytes;  // 2 buffers (unit parity)
 constexpr int kOffPt = kOffQp + 2 * kFtOpBytes;            // 2 buffers (tile parity) of 2 halves
 constexpr int kOffX = kOffPt + 4 * kFtOpBytes;             // float [2][4 warps][8]: exchanges
-constexpr int kOffBar = kOffX + 2 * 4 * 8 * 4;
+constexpr int kOffKn = kOffX + 2 * 4 * 8 * 4;              // fused append: 2 new K rows (unit parity), E4M3
+constexpr int kOffKnAt = kOffKn + 2 * kHeadDim;            // int [2]: where each row goes (tile << 8 | row), or -1
+constexpr int kOffBar = kOffKnAt + 16;
 constexpr int kSmemFt = kOffBar + 512;
 constexpr uint32_t kColS = 0;    // S^T buffers at columns 0 and 32 (16 columns per half)
 constexpr uint32_t kColO = 64;   // O^T buffers at columns 64 and 80
@@ -88,6 +90,7 @@ constexpr float kFtLn2 = 0.6931471805599453f;
 constexpr int kFtNamedBar = 1;          // the softmax warps' barrier
 
 static_assert(kSmemFt <= 227 * 1024, "one CTA per SM");
+static_assert(kFtTileTokens == 2 * 128, "a tile is two 128-token MMA halves");
 static_assert(kOffV % 1024 == 0 && kOffQp % 1024 == 0 && kOffPt % 1024 == 0 && kFtOpBytes % 1024 == 0,
               "swizzled operands need 1 KiB alignment");
 static_assert(kFtLazyMax + 6.f <= 8.f, "scaled weights must stay inside E4M3's range");
@@ -111,6 +114,10 @@ static_assert(sizeof(FtBars) <= 512, "barrier area");
 
 struct FtUnit {
   int r, kvh, split, b0, b1, n_tiles, ctx_keys, ctx_raw;
+  // fused append: the tile and tile row holding the request's new token
+  // (position ctx - 1) and its logical block; new_tile = -1 when the unit
+  // does not hold it or there is no append
+  int new_tile, new_row, new_blk;
 };
 
 // Unit u: split fastest, then KV head, then request.
@@ -127,7 +134,35 @@ __device__ __forceinline__ FtUnit ft_unit(const DecodeArgs& a, int u) {
   x.b1 = min(nb, x.b0 + a.blocks_per_split);
   x.n_tiles = x.b1 > x.b0 ? (x.b1 - x.b0 + kFtTileBlocks - 1) / kFtTileBlocks : 0;
   x.ctx_keys = min(ctx, x.b1 * kBlockSize);
+  x.new_tile = -1;
+  x.new_row = 0;
+  x.new_blk = 0;
+  if (a.k_new != nullptr && x.ctx_raw > 0 && x.ctx_raw <= a.max_blocks * kBlockSize) {
+    const int p = x.ctx_raw - 1;
+    const int nbl = p / kBlockSize;
+    if (nbl >= x.b0 && nbl < x.b1) {
+      x.new_tile = (nbl - x.b0) / kFtTileBlocks;
+      x.new_row = ((nbl - x.b0) % kFtTileBlocks) * kBlockSize + p % kBlockSize;
+      x.new_blk = nbl;
+    }
+  }
   return x;
+}
+
+// Fused append: the caller's slot for the unit's new token, and whether it is
+// the slot the block table gives that position (only then is the row patched
+// into the tiles; any slot inside the pool is stored, as the append would).
+__device__ __forceinline__ bool ft_new_slot(const DecodeArgs& a, const FtUnit& x, int64_t& slot) {
+  slot = a.slot_mapping[x.r];
+  const int pb = a.block_tables[static_cast<int64_t>(x.r) * a.max_blocks + x.new_blk];
+  return slot >= 0 && slot == static_cast<int64_t>(pb) * kBlockSize + (x.ctx_raw - 1) % kBlockSize;
+}
+
+// Byte offset of the 4 E4M3 values of dims 4l .. 4l+3 of a 256-token stage's
+// row `row` (two 128-row halves, 128-byte swizzle).
+__device__ __forceinline__ uint32_t ft_row_word(int row, int l) {
+  const int half = row >> 7, r = row & 127;
+  return half * kFtHalfBytes + r * 128 + ((((l >> 2) ^ (r & 7)) & 7) << 4) + (l & 3) * 4;
 }
 
 // Producer warp: TMA loads of one tensor's tiles into its ring.  Lane b < 16
@@ -200,6 +235,11 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t pair, float& lo, float&
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(p));
   lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
   hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
+// 4 BF16 values (two words) as 4 E4M3 bytes, rounded as the E4M3 append rounds.
+__device__ __forceinline__ uint32_t bf16x4_to_e4m3x4(uint32_t w0, uint32_t w1) {
+  return f32x2_to_e4m3x2(bf16_hi(w0), bf16_lo(w0)) | (f32x2_to_e4m3x2(bf16_hi(w1), bf16_lo(w1)) << 16);
 }
 
 // The power of two that brings a head's largest |q| (BF16 magnitude bits
@@ -300,6 +340,9 @@ __global__ void __launch_bounds__(kFtThreads, 1)
       settle(cs);
       Cursor cp = cs;
       uint64_t t_idle = 0;
+      // fused append, K side: the S cursor's unit's new K row (tile << 8 | tile
+      // row, or -1), published with the unit's query operand
+      int kp_at = -1;
       while (cp.u < num_units) {
         bool progressed = false;
         // ---- S of the next tile ----
@@ -312,6 +355,17 @@ __global__ void __launch_bounds__(kFtThreads, 1)
             tc::fence_after_sync();
             const uint32_t kst = sbase + kOffK + st * kFtStageBytes;
             const uint32_t qp = sbase + kOffQp + ub * kFtOpBytes;
+            if (cs.j == 0) kp_at = a.k_new != nullptr ? reinterpret_cast<const int*>(smem + kOffKnAt)[ub] : -1;
+            if (kp_at >= 0 && (kp_at >> 8) == cs.j) {
+              // the new token's K row (E4M3, from the query-operand warp)
+              // written over the tile's row, 16-byte chunks to their swizzled places
+              const int row = kp_at & 255, r = row & 127;
+              const uint4* src = reinterpret_cast<const uint4*>(smem + kOffKn + ub * kHeadDim);
+              uint8_t* dst = smem + kOffK + st * kFtStageBytes + (row >> 7) * kFtHalfBytes + r * 128;
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch) *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) << 4)) = src[ch];
+              tc::fence_proxy_async_smem();  // the tensor core reads the patched row
+            }
 #pragma unroll
             for (int half = 0; half < 2; ++half)
 #pragma unroll
@@ -405,11 +459,40 @@ __global__ void __launch_bounds__(kFtThreads, 1)
         hi[k] = h01 | (h23 << 16);
         lo[k] = f32x2_to_e4m3x2(rv[1], rv[0]) | (f32x2_to_e4m3x2(rv[3], rv[2]) << 16);
       }
+      // fused append, K side: lane l rounds dims 4l .. 4l+3 of the unit's new
+      // K row to E4M3 as the append rounds and stores them where the append
+      // would; the row goes to the MMA thread with the query operand, which
+      // writes it over the tile's row
+      int kn_at = -1;
+      uint32_t kn_word = 0;
+      if (x.new_tile >= 0) {
+        int64_t slot;
+        const bool patch = ft_new_slot(a, x, slot);
+        if (slot >= 0) {
+          const uint2 k = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.k_new) +
+                                                         (static_cast<int64_t>(x.r) * a.num_kv_heads + x.kvh) *
+                                                             kHeadDim)[lane];
+          kn_word = bf16x4_to_e4m3x4(k.x, k.y);
+          if (slot < static_cast<int64_t>(a.num_blocks) * kBlockSize)
+            *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(const_cast<void*>(a.k_cache)) +
+                                         ((slot / kBlockSize) * a.num_kv_heads + x.kvh) *
+                                             static_cast<int64_t>(kFtBoxBytes) +
+                                         (slot % kBlockSize) * kHeadDim + 4 * lane) = kn_word;
+          if (patch)
+            kn_at = (x.new_tile << 8) | x.new_row;
+          else if (lane == 0)
+            report(a.err, PKV_DEVERR_SLOT);
+        }
+      }
       if (seq >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_empty[ub], ((seq >> 1) - 1) & 1));
       if (!ok) break;
       uint8_t* dst = smem + kOffQp + ub * kFtOpBytes;
       *reinterpret_cast<uint4*>(dst + tc::sw128_offset_b8(h, 16 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(dst + tc::sw128_offset_b8(4 + h, 16 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      if (a.k_new != nullptr) {
+        reinterpret_cast<uint32_t*>(smem + kOffKn + ub * kHeadDim)[lane] = kn_word;
+        if (lane == 0) reinterpret_cast<int*>(smem + kOffKnAt)[ub] = kn_at;
+      }
       tc::fence_proxy_async_smem();
       mbar_arrive(&bars->q_full[ub]);
       ++seq;
@@ -469,6 +552,20 @@ __global__ void __launch_bounds__(kFtThreads, 1)
         const float inv_sigma = 1.f / q_sigma(amax);  // a power of two: exact
 #pragma unroll
         for (int h = 0; h < 4; ++h) c[h] = a.scale_log2 * __shfl_sync(0xffffffffu, inv_sigma, 8 * h);
+      }
+      // fused append, V side: the warp whose lanes own the new token's tile
+      // row loads its V row (lane l: dims 4l .. 4l+3, rounded to E4M3 as the
+      // append rounds) and writes it once that tile's V has landed
+      bool vp_mine = false, vp_patch = false;
+      int64_t vp_slot = -1;
+      uint32_t vp_word = 0;
+      if (x.new_tile >= 0 && ((x.new_row & 127) >> 5) == w) {
+        vp_patch = ft_new_slot(a, x, vp_slot);
+        vp_mine = vp_slot >= 0;
+        const uint2 v = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.v_new) +
+                                                       (static_cast<int64_t>(x.r) * a.num_kv_heads + x.kvh) *
+                                                           kHeadDim)[lane];
+        vp_word = bf16x4_to_e4m3x4(v.x, v.y);
       }
       float m[4], l[4];
 #pragma unroll
@@ -576,7 +673,8 @@ __global__ void __launch_bounds__(kFtThreads, 1)
         bool garbage[2];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) garbage[hf] = !valid[hf] && tok0 + 128 * hf < x.b1 * kBlockSize;
-        if (ok && __any_sync(0xffffffffu, garbage[0] || garbage[1])) {
+        const bool vp_now = vp_mine && j == x.new_tile;  // warp-uniform
+        if (ok && (vp_now || __any_sync(0xffffffffu, garbage[0] || garbage[1]))) {
           const int st = i % kFtStages;
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (i / kFtStages) & 1));
 #pragma unroll
@@ -586,6 +684,17 @@ __global__ void __launch_bounds__(kFtThreads, 1)
 #pragma unroll
               for (int cc = 0; cc < 8; ++cc) vrow[cc] = make_uint4(0, 0, 0, 0);
             }
+          if (ok && vp_now) {
+            // the new token's V row, stored where the append would and written over the tile's row
+            if (vp_slot < static_cast<int64_t>(a.num_blocks) * kBlockSize)
+              *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(const_cast<void*>(a.v_cache)) +
+                                           ((vp_slot / kBlockSize) * a.num_kv_heads + x.kvh) *
+                                               static_cast<int64_t>(kFtBoxBytes) +
+                                           (vp_slot % kBlockSize) * kHeadDim + 4 * lane) = vp_word;
+            if (vp_patch)
+              *reinterpret_cast<uint32_t*>(smem + kOffV + st * kFtStageBytes + ft_row_word(x.new_row, lane)) =
+                  vp_word;
+          }
         }
         if (ok) {
 #pragma unroll

@@ -624,7 +624,7 @@ pkv_status quantised_attention(void* out, const void* q, const void* k_cache, co
                                const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
                                const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
                                int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes, void* stream,
-                               bool fp8) {
+                               bool fp8, const FusedAppend* fused = nullptr, bool dry_run = false) {
   pkv_status st = check_cache(cache);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_blocks_per_seq < 1 || kv_blocks_per_split < 0) return PKV_ERR_SHAPE;
@@ -662,6 +662,11 @@ pkv_status quantised_attention(void* out, const void* q, const void* k_cache, co
   a.num_splits = splits;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.part_slots = splits;
+  if (fused != nullptr) {  // E4M3 only: the decode kernel stores the new tokens
+    a.slot_mapping = fused->slot_mapping;
+    a.k_new = fused->k_new;
+    a.v_new = fused->v_new;
+  }
   const int sms = device_sm_count();
   const int32_t grid = static_cast<int32_t>(units < sms ? units : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -670,10 +675,14 @@ pkv_status quantised_attention(void* out, const void* q, const void* k_cache, co
   auto launch = [&]() {
     return fp8 ? launch_paged_decode_fp8_tc(a, grid, s) : launch_paged_decode_q8(a, grid, s);
   };
-  if (splits == 1) return launch() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  if (splits == 1) {
+    if (dry_run) return PKV_OK;
+    return launch() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
   const size_t need = pkv_workspace_size_q8_0(num_seqs, num_q_heads, max_blocks_per_seq, bps);
   if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+  if (dry_run) return PKV_OK;
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
@@ -707,6 +716,41 @@ pkv_status pkv_paged_attention_fp8_e4m3(void* out, const void* q, const void* k_
   return quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
                              num_seqs, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream,
                              true);
+}
+
+pkv_status pkv_paged_attention_fp8_e4m3_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                               const pkv_cache_desc* cache, const int32_t* block_tables,
+                                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                               int32_t num_seqs, int32_t num_q_heads, float scale,
+                                               int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
+                                               const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                                               int32_t num_tokens, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens > 0) {
+    if (!k_cache || !v_cache || !slot_mapping || !k_new || !v_new) return PKV_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+         reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+      return PKV_ERR_UNSUPPORTED;
+  }
+  // every check of the attention first, so an error enqueues nothing
+  st = quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                           num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream, true, nullptr,
+                           true);
+  if (st != PKV_OK) return st;
+  if (num_tokens == num_seqs && num_seqs > 0) {  // token r is request r's new token: one launch
+    const FusedAppend f{slot_mapping, k_new, v_new};
+    return quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                               num_seqs, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream,
+                               true, &f, false);
+  }
+  if (num_tokens > 0) {
+    st = pkv_kv_append_fp8_e4m3(k_cache, v_cache, cache, slot_mapping, k_new, v_new, num_tokens, stream);
+    if (st != PKV_OK) return st;
+  }
+  return quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                             num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream, true);
 }
 
 pkv_status pkv_kv_append_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cache_desc* cache,

@@ -203,3 +203,97 @@ def test_fused_random_shapes(seed):
     w.slot_mapping[rng.random(b) < 0.1] = -1
     bps = int(rng.choice([0, 0, 3, 16, 40, 1000]))
     _assert_same(_both(w, bps), f"random seed={seed} b={b} bps={bps}")
+
+
+def _fp8_pools(d, w):
+    """E4M3 pools holding the workload's BF16 cache, stored through the E4M3 append."""
+    nb, hkv = w.num_blocks, w.num_kv_heads
+    tok = lambda t: t.permute(0, 2, 1, 3).contiguous().view(nb * 16, hkv, 128)
+    kq = torch.empty((nb, hkv, 16, 128), dtype=torch.uint8, device="cuda")
+    vq = torch.empty_like(kq)
+    pkv.kv_append_fp8_e4m3(kq, vq, torch.arange(nb * 16, dtype=torch.int64, device="cuda"), tok(d["k_cache"]),
+                           tok(d["v_cache"]))
+    return kq, vq
+
+
+def _fp8_both(w, bps=0):
+    d = to_device(w)
+    kq, vq = _fp8_pools(d, w)
+    maxb = w.max_blocks_per_seq
+    if bps == 0:
+        bps = pkv.choose_kv_blocks_per_split_fp8_e4m3(w.num_seqs, w.num_kv_heads, maxb)
+    ws = torch.empty(max(pkv.workspace_size_q8_0(w.num_seqs, w.num_q_heads, maxb, bps), 256), dtype=torch.uint8,
+                     device="cuda")
+    res = []
+    for fused in (True, False):
+        kc, vc = kq.clone(), vq.clone()
+        out = torch.full_like(d["q"], float("nan"))
+        if fused:
+            pkv.paged_attention_fp8_e4m3_append(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
+                                                d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=bps,
+                                                workspace=ws)
+        else:
+            pkv.kv_append_fp8_e4m3(kc, vc, d["slot_mapping"], d["k_new"], d["v_new"])
+            pkv.paged_attention_fp8_e4m3(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
+                                         kv_blocks_per_split=bps, workspace=ws)
+        torch.cuda.synchronize()
+        res.append((out, kc, vc))
+    return res
+
+
+def _assert_same_fp8(res, what):
+    (of, kf, vf), (os_, ks, vs) = res
+    assert torch.equal(of.view(torch.int16), os_.view(torch.int16)), f"{what}: outputs differ"
+    assert torch.equal(kf, ks) and torch.equal(vf, vs), f"{what}: E4M3 pools differ"
+
+
+# new tokens in the first and second 128-row half of a 256-token tile, at a block's first and last
+# slot, alone, and a padding row
+RAGGED_FP8 = [17, 300, 1, 16, 700, 0, 32, 2049, 129, 200, 4000]
+
+
+@pytest.mark.parametrize("bps", [0, 8, 24, 5, 1000])
+def test_fused_fp8_equals_append_then_attention(bps):
+    ctx = np.asarray(RAGGED_FP8)
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("fused-fp8", ctx, need + 30, seed=71)
+    _assert_same_fp8(_fp8_both(w, bps), f"fused fp8 bps={bps}")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fused_fp8_random_shapes(seed):
+    rng = np.random.default_rng(3000 + seed)
+    b = int(rng.integers(1, 61))
+    ctx = rng.integers(0, 3001, size=b)
+    ctx[rng.random(b) < 0.1] = 0
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("fused-fp8-rand", ctx, need + 16, seed=4000 + seed)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[rng.random(b) < 0.1] = -1
+    bps = int(rng.choice([0, 0, 5, 16, 40, 1000]))
+    _assert_same_fp8(_fp8_both(w, bps), f"fp8 random seed={seed} b={b} bps={bps}")
+
+
+def test_fused_fp8_wrong_slot_sets_the_error_word():
+    ctx = np.asarray([100, 200, 300])
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("bad-slot-fp8", ctx, need + 30, seed=72)
+    used = set()
+    for r, c in enumerate(ctx):
+        used.update(int(b) for b in w.block_tables[r, :-(-int(c) // 16)])
+    spare = next(b for b in range(w.num_blocks) if b not in used)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[2] = spare * 16 + 5
+    d = to_device(w)
+    kq, vq = _fp8_pools(d, w)
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(d["q"])
+    pkv.paged_attention_fp8_e4m3_append(out, d["q"], kq, vq, d["block_tables"], d["context_lens"], w.scale,
+                                        d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=1000,
+                                        workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(reset=True) == pkv.DEVERR_SLOT
+    ref_k, ref_v = kq.clone(), vq.clone()
+    pkv.kv_append_fp8_e4m3(ref_k, ref_v, d["slot_mapping"], d["k_new"], d["v_new"])
+    torch.cuda.synchronize()
+    assert torch.equal(kq[spare], ref_k[spare]) and torch.equal(vq[spare], ref_v[spare])  # stored as the append would
