@@ -120,7 +120,9 @@ struct FtUnit {
   int new_tile, new_row, new_blk;
 };
 
-// Unit u: split fastest, then KV head, then request.
+// Unit u: split fastest, then KV head, then request.  kFused: also where the
+// request's new token falls (the fused append).
+template <bool kFused>
 __device__ __forceinline__ FtUnit ft_unit(const DecodeArgs& a, int u) {
   FtUnit x;
   x.split = u % a.num_splits;
@@ -137,7 +139,7 @@ __device__ __forceinline__ FtUnit ft_unit(const DecodeArgs& a, int u) {
   x.new_tile = -1;
   x.new_row = 0;
   x.new_blk = 0;
-  if (a.k_new != nullptr && x.ctx_raw > 0 && x.ctx_raw <= a.max_blocks * kBlockSize) {
+  if (kFused && x.ctx_raw > 0 && x.ctx_raw <= a.max_blocks * kBlockSize) {
     const int p = x.ctx_raw - 1;
     const int nbl = p / kBlockSize;
     if (nbl >= x.b0 && nbl < x.b1) {
@@ -175,7 +177,7 @@ __device__ __forceinline__ bool ft_produce(const DecodeArgs& a, const CUtensorMa
   bool ok = true;
   int i = 0;
   for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-    const FtUnit x = ft_unit(a, u);
+    const FtUnit x = ft_unit<false>(a, u);
     if (x.n_tiles == 0) continue;
     const int32_t* table = a.block_tables + static_cast<int64_t>(x.r) * a.max_blocks;
     // the load stays inside the table row whatever the context length, so it
@@ -253,6 +255,10 @@ __device__ __forceinline__ float q_sigma(uint32_t amax_bits) {
   return __int_as_float((127 + s) << 23);
 }
 
+// kFused: the request's new token is stored and used in place of the row
+// read (a.k_new, a.v_new, a.slot_mapping set); an instance of its own, so the
+// plain decode carries none of that work.
+template <bool kFused>
 __global__ void __launch_bounds__(kFtThreads, 1)
     paged_decode_fp8_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                                const DecodeArgs a) {
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(kFtThreads, 1)
       };
       auto settle = [&](Cursor& c) {  // move to the first unit with a tile, from c.u on
         for (; c.u < num_units; c.u += gridDim.x) {
-          c.n = ft_unit(a, c.u).n_tiles;
+          c.n = ft_unit<false>(a, c.u).n_tiles;
           if (c.n > 0) return;
         }
       };
@@ -355,8 +361,8 @@ __global__ void __launch_bounds__(kFtThreads, 1)
             tc::fence_after_sync();
             const uint32_t kst = sbase + kOffK + st * kFtStageBytes;
             const uint32_t qp = sbase + kOffQp + ub * kFtOpBytes;
-            if (cs.j == 0) kp_at = a.k_new != nullptr ? reinterpret_cast<const int*>(smem + kOffKnAt)[ub] : -1;
-            if (kp_at >= 0 && (kp_at >> 8) == cs.j) {
+            if (kFused && cs.j == 0) kp_at = reinterpret_cast<const int*>(smem + kOffKnAt)[ub];
+            if (kFused && kp_at >= 0 && (kp_at >> 8) == cs.j) {
               // the new token's K row (E4M3, from the query-operand warp)
               // written over the tile's row, 16-byte chunks to their swizzled places
               const int row = kp_at & 255, r = row & 127;
@@ -425,13 +431,26 @@ __global__ void __launch_bounds__(kFtThreads, 1)
     const int h = lane >> 3, c = lane & 7;
     int seq = 0;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const FtUnit x = ft_unit(a, u);
+      const FtUnit x = ft_unit<kFused>(a, u);
       if (x.n_tiles == 0) continue;
       const int ub = seq & 1;
       const uint4* src = reinterpret_cast<const uint4*>(
           static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(x.r) * hq + x.kvh * kGroup + h) * kHeadDim +
           16 * c);
       const uint4 w0 = src[0], w1 = src[1];
+      // fused append, K side: lane l rounds dims 4l .. 4l+3 of the unit's new
+      // K row to E4M3 as the append rounds and stores them where the append
+      // would; the row goes to the MMA thread with the query operand, which
+      // writes it over the tile's row.  The row is loaded with the slot, not
+      // after it, so it costs no extra round trip before the first tile.
+      uint2 kraw = make_uint2(0, 0);
+      int64_t kslot = -1;
+      bool kpatch = false;
+      if (kFused && x.new_tile >= 0) {
+        kraw = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.k_new) +
+                                              (static_cast<int64_t>(x.r) * a.num_kv_heads + x.kvh) * kHeadDim)[lane];
+        kpatch = ft_new_slot(a, x, kslot);
+      }
       const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
       uint32_t amax = 0;
 #pragma unroll
@@ -459,37 +478,26 @@ __global__ void __launch_bounds__(kFtThreads, 1)
         hi[k] = h01 | (h23 << 16);
         lo[k] = f32x2_to_e4m3x2(rv[1], rv[0]) | (f32x2_to_e4m3x2(rv[3], rv[2]) << 16);
       }
-      // fused append, K side: lane l rounds dims 4l .. 4l+3 of the unit's new
-      // K row to E4M3 as the append rounds and stores them where the append
-      // would; the row goes to the MMA thread with the query operand, which
-      // writes it over the tile's row
       int kn_at = -1;
       uint32_t kn_word = 0;
-      if (x.new_tile >= 0) {
-        int64_t slot;
-        const bool patch = ft_new_slot(a, x, slot);
-        if (slot >= 0) {
-          const uint2 k = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.k_new) +
-                                                         (static_cast<int64_t>(x.r) * a.num_kv_heads + x.kvh) *
-                                                             kHeadDim)[lane];
-          kn_word = bf16x4_to_e4m3x4(k.x, k.y);
-          if (slot < static_cast<int64_t>(a.num_blocks) * kBlockSize)
-            *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(const_cast<void*>(a.k_cache)) +
-                                         ((slot / kBlockSize) * a.num_kv_heads + x.kvh) *
-                                             static_cast<int64_t>(kFtBoxBytes) +
-                                         (slot % kBlockSize) * kHeadDim + 4 * lane) = kn_word;
-          if (patch)
-            kn_at = (x.new_tile << 8) | x.new_row;
-          else if (lane == 0)
-            report(a.err, PKV_DEVERR_SLOT);
-        }
+      if (kFused && kslot >= 0) {
+        kn_word = bf16x4_to_e4m3x4(kraw.x, kraw.y);
+        if (kslot < static_cast<int64_t>(a.num_blocks) * kBlockSize)
+          *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(const_cast<void*>(a.k_cache)) +
+                                       ((kslot / kBlockSize) * a.num_kv_heads + x.kvh) *
+                                           static_cast<int64_t>(kFtBoxBytes) +
+                                       (kslot % kBlockSize) * kHeadDim + 4 * lane) = kn_word;
+        if (kpatch)
+          kn_at = (x.new_tile << 8) | x.new_row;
+        else if (lane == 0)
+          report(a.err, PKV_DEVERR_SLOT);
       }
       if (seq >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_empty[ub], ((seq >> 1) - 1) & 1));
       if (!ok) break;
       uint8_t* dst = smem + kOffQp + ub * kFtOpBytes;
       *reinterpret_cast<uint4*>(dst + tc::sw128_offset_b8(h, 16 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(dst + tc::sw128_offset_b8(4 + h, 16 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      if (a.k_new != nullptr) {
+      if (kFused) {
         reinterpret_cast<uint32_t*>(smem + kOffKn + ub * kHeadDim)[lane] = kn_word;
         if (lane == 0) reinterpret_cast<int*>(smem + kOffKnAt)[ub] = kn_at;
       }
@@ -523,7 +531,7 @@ __global__ void __launch_bounds__(kFtThreads, 1)
     };
     int i = 0, seq = 0;
     for (int u = blockIdx.x; u < num_units && ok_all; u += gridDim.x) {
-      const FtUnit x = ft_unit(a, u);
+      const FtUnit x = ft_unit<kFused>(a, u);
       const int64_t orow0 = static_cast<int64_t>(x.r) * hq + x.kvh * kGroup;
       if (threadIdx.x == 128 && x.split == 0 && x.kvh == 0 && x.ctx_raw > a.max_blocks * kBlockSize)
         report(a.err, PKV_DEVERR_CONTEXT);
@@ -559,7 +567,7 @@ __global__ void __launch_bounds__(kFtThreads, 1)
       bool vp_mine = false, vp_patch = false;
       int64_t vp_slot = -1;
       uint32_t vp_word = 0;
-      if (x.new_tile >= 0 && ((x.new_row & 127) >> 5) == w) {
+      if (kFused && x.new_tile >= 0 && ((x.new_row & 127) >> 5) == w) {
         vp_patch = ft_new_slot(a, x, vp_slot);
         vp_mine = vp_slot >= 0;
         const uint2 v = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.v_new) +
@@ -776,6 +784,7 @@ __global__ void __launch_bounds__(kFtThreads, 1)
   }
 }
 
+template <bool kFused>
 cudaError_t allow_smem_ft() {
   static bool done[64];
   int dev = 0;
@@ -783,7 +792,8 @@ cudaError_t allow_smem_ft() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev]) {
-    e = cudaFuncSetAttribute(paged_decode_fp8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemFt);
+    e = cudaFuncSetAttribute(paged_decode_fp8_tc_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemFt);
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
@@ -801,10 +811,14 @@ cudaError_t launch_paged_decode_fp8_tc(const DecodeArgs& a, int32_t grid, cudaSt
   CUtensorMap kmap, vmap;
   if (!make_pool_map_e4m3(&kmap, a.k_cache, rows) || !make_pool_map_e4m3(&vmap, a.v_cache, rows))
     return cudaErrorInvalidValue;
-  cudaError_t e = allow_smem_ft();
+  const bool fused = a.k_new != nullptr;
+  if (fused && (a.v_new == nullptr || a.slot_mapping == nullptr)) return cudaErrorInvalidValue;
+  cudaError_t e = fused ? allow_smem_ft<true>() : allow_smem_ft<false>();
   if (e != cudaSuccess) return e;
-  return launch_pdl(paged_decode_fp8_tc_kernel, dim3(static_cast<unsigned>(grid)), dim3(kFtThreads), kSmemFt,
-                    stream, 1, kmap, vmap, a);
+  return fused ? launch_pdl(paged_decode_fp8_tc_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kFtThreads),
+                            kSmemFt, stream, 1, kmap, vmap, a)
+               : launch_pdl(paged_decode_fp8_tc_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kFtThreads),
+                            kSmemFt, stream, 1, kmap, vmap, a);
 }
 
 }  // namespace pkv
