@@ -234,3 +234,21 @@ def test_paged_attention_append_argument_errors():
              None) == 1
     assert f(None, None, 4096, 4096, ctypes.byref(d), None, 1, None, 1, 1, 32, 1.0, 0, None, 0, 4096, 4100, 4096, 1,
              None) == 3  # k_new not 16-byte aligned
+
+
+def test_paged_attention_fp8_e4m3_append_argument_errors():
+    """The E4M3 append-and-attention call checks its own arguments on the
+    host before anything else (no CUDA call on these paths)."""
+    f = pkv.lib().pkv_paged_attention_fp8_e4m3_append
+    d = _desc()
+    # no cache descriptor; a negative token count; new tokens without their K; a misaligned K
+    assert f(None, None, None, None, None, None, 1, None, 1, 32, 1.0, 0, None, 0, None, None, None, 0, None) == 1
+    assert f(None, None, None, None, ctypes.byref(d), None, 1, None, 1, 32, 1.0, 0, None, 0, None, None, None, -1,
+             None) == 2
+    assert f(None, None, 4096, 4096, ctypes.byref(d), None, 1, None, 1, 32, 1.0, 0, None, 0, 4096, None, 4096, 1,
+             None) == 1
+    assert f(None, None, 4096, 4096, ctypes.byref(d), None, 1, None, 1, 32, 1.0, 0, None, 0, 4096, 4100, 4096, 1,
+             None) == 3
+    # the attention's own checks run before anything is enqueued: no query
+    assert f(None, None, 4096, 4096, ctypes.byref(d), 4096, 1, 4096, 1, 32, 1.0, 0, None, 0, 4096, 4096, 4096, 1,
+             None) == 1
