@@ -297,3 +297,38 @@ def test_fused_fp8_wrong_slot_sets_the_error_word():
     pkv.kv_append_fp8_e4m3(ref_k, ref_v, d["slot_mapping"], d["k_new"], d["v_new"])
     torch.cuda.synchronize()
     assert torch.equal(kq[spare], ref_k[spare]) and torch.equal(vq[spare], ref_v[spare])  # stored as the append would
+
+
+def test_fused_fp8_short_chat_full_size():
+    """The 2K-context batch at full size (37 requests, 5461-block pools filled
+    on the device) in the launch configuration of the benchmark's step (the
+    library's split choice): the fused call equals the E4M3 append followed by
+    the attention, outputs and pools bit for bit."""
+    w = W.short_chat(seed=21, fill_cache=False)
+    nb, hkv = w.num_blocks, w.num_kv_heads
+    kb = torch.empty((nb, hkv, 16, 128), dtype=torch.bfloat16, device="cuda")
+    vb = torch.empty_like(kb)
+    W.fill_pool_device(kb, seed=21)
+    W.fill_pool_device(vb, seed=22)
+    tok = lambda p: p.permute(0, 2, 1, 3).contiguous().view(nb * 16, hkv, 128)
+    kq = torch.empty((nb, hkv, 16, 128), dtype=torch.uint8, device="cuda")
+    vq = torch.empty_like(kq)
+    pkv.kv_append_fp8_e4m3(kq, vq, torch.arange(nb * 16, dtype=torch.int64, device="cuda"), tok(kb), tok(vb))
+    del kb, vb
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q, kn, vn = (dev(x).view(torch.bfloat16) for x in (w.q, w.k_new, w.v_new))
+    tables, ctx, slots = dev(w.block_tables), dev(w.context_lens), dev(w.slot_mapping)
+    maxb = w.max_blocks_per_seq
+    bps = pkv.choose_kv_blocks_per_split_fp8_e4m3(w.num_seqs, hkv, maxb)
+    ws = torch.empty(max(pkv.workspace_size_q8_0(w.num_seqs, w.num_q_heads, maxb, bps), 256), dtype=torch.uint8,
+                     device="cuda")
+    kf, vf = kq.clone(), vq.clone()
+    out_s, out_f = torch.full_like(q, float("nan")), torch.full_like(q, float("nan"))
+    pkv.kv_append_fp8_e4m3(kq, vq, slots, kn, vn)
+    pkv.paged_attention_fp8_e4m3(out_s, q, kq, vq, tables, ctx, w.scale, kv_blocks_per_split=bps, workspace=ws)
+    pkv.paged_attention_fp8_e4m3_append(out_f, q, kf, vf, tables, ctx, w.scale, slots, kn, vn,
+                                        kv_blocks_per_split=bps, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_f.view(torch.int16), out_s.view(torch.int16)), "full-size fp8: outputs differ"
+    assert torch.equal(kf, kq) and torch.equal(vf, vq), "full-size fp8: pools differ"
+    assert torch.isfinite(out_f.float()).all()
