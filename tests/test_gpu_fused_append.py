@@ -332,3 +332,34 @@ def test_fused_fp8_short_chat_full_size():
     assert torch.equal(out_f.view(torch.int16), out_s.view(torch.int16)), "full-size fp8: outputs differ"
     assert torch.equal(kf, kq) and torch.equal(vf, vq), "full-size fp8: pools differ"
     assert torch.isfinite(out_f.float()).all()
+
+
+def test_fused_bf16_short_chat_full_size():
+    """The benchmark's default step at full size (37 requests, 5461-block BF16
+    pools filled on the device, the library's split choice): the fused call
+    equals the append followed by the attention, outputs and pools bit for
+    bit."""
+    w = W.short_chat(seed=23, fill_cache=False)
+    nb, hkv = w.num_blocks, w.num_kv_heads
+    kc = torch.empty((nb, hkv, 16, 128), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    W.fill_pool_device(kc, seed=23)
+    W.fill_pool_device(vc, seed=24)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q, kn, vn = (dev(x).view(torch.bfloat16) for x in (w.q, w.k_new, w.v_new))
+    tables, ctx, slots = dev(w.block_tables), dev(w.context_lens), dev(w.slot_mapping)
+    maxb = w.max_blocks_per_seq
+    bps = pkv.choose_kv_blocks_per_split(w.num_seqs, hkv, 1, maxb)
+    ws = torch.empty(max(pkv.workspace_size(w.num_seqs, 1, w.num_q_heads, maxb, bps), 256), dtype=torch.uint8,
+                     device="cuda")
+    kf, vf = kc.clone(), vc.clone()
+    out_s, out_f = torch.full_like(q, float("nan")), torch.full_like(q, float("nan"))
+    pkv.kv_append(kc, vc, slots, kn, vn)
+    pkv.paged_attention(out_s, q, kc, vc, tables, ctx, 1, w.scale, kv_blocks_per_split=bps, workspace=ws)
+    pkv.paged_attention_append(out_f, q, kf, vf, tables, ctx, 1, w.scale, slots, kn, vn, kv_blocks_per_split=bps,
+                               workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_f.view(torch.int16), out_s.view(torch.int16)), "full-size bf16: outputs differ"
+    assert torch.equal(kf.view(torch.int16), kc.view(torch.int16)) and \
+        torch.equal(vf.view(torch.int16), vc.view(torch.int16)), "full-size bf16: pools differ"
+    assert torch.isfinite(out_f.float()).all()
