@@ -1,14 +1,20 @@
 """pkv_decode_graph_*: a decode step of several layers (per layer: append the
 step's new tokens, then attention) captured as one CUDA graph per buffer set.
-The graphs run the very kernels of the direct calls, so after the same
-sequence of steps -- buffer set 0, set 1, set 0 again -- their outputs and the
-layers' pools must equal the direct calls' bit for bit, for every KV format,
-the cascade and a query chunk."""
+After the same sequence of steps -- buffer set 0, set 1, set 0 again -- the
+graphs' outputs and the layers' pools must
+  * equal the direct calls' bit for bit (the graphs run the very kernels of
+    the direct calls), and
+  * match the FP64 oracle replaying the same steps on host copies: pools
+    bit-exact (the oracle's append, BF16 / q8_0 / E4M3), every layer's output
+    of both buffer sets within the attention tolerance,
+for every KV format, the cascade and query chunks."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
+from gpu_util import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -34,12 +40,18 @@ def _dev_bf16(a: np.ndarray) -> torch.Tensor:
 
 
 def _buffer_set(w, rng, cascade):
-    """One step's buffers: per-layer queries and new K/V; slots, tables and lengths shared by the layers."""
+    """One step's buffers: per-layer queries and new K/V; slots, tables and lengths shared by the layers.
+    Returns (device buffers, host copies of the per-layer values)."""
     b, ql, hq, hkv, t = w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, w.slot_mapping.size
+    host = {
+        "q": W.randn_bf16(rng, (LAYERS, b, ql, hq, 128)),
+        "k_new": W.randn_bf16(rng, (LAYERS, t, hkv, 128)),
+        "v_new": W.randn_bf16(rng, (LAYERS, t, hkv, 128)),
+    }
     st = {
-        "q": _dev_bf16(W.randn_bf16(rng, (LAYERS, b, ql, hq, 128))),
-        "k_new": _dev_bf16(W.randn_bf16(rng, (LAYERS, t, hkv, 128))),
-        "v_new": _dev_bf16(W.randn_bf16(rng, (LAYERS, t, hkv, 128))),
+        "q": _dev_bf16(host["q"]),
+        "k_new": _dev_bf16(host["k_new"]),
+        "v_new": _dev_bf16(host["v_new"]),
         "slot_mapping": torch.from_numpy(w.slot_mapping).cuda(),
         "block_tables": torch.from_numpy(w.block_tables).cuda(),
         "context_lens": torch.from_numpy(w.context_lens).cuda(),
@@ -49,32 +61,64 @@ def _buffer_set(w, rng, cascade):
         gs, gb, sp = cascade
         st.update(group_seqs=torch.from_numpy(gs).cuda(), group_blocks=torch.from_numpy(gb).cuda(),
                   seq_prefix_blocks=torch.from_numpy(sp).cuda())
-    return st
+    return st, host
 
 
-def _pools(fmt, w, seed):
-    """Per-layer K and V pools of the format, every slot holding seeded values."""
+def _host_pools(fmt, w, seed):
+    """Per-layer K and V pools of the format, every slot holding seeded N(0,1)
+    values; the quantised formats are stored by the oracle's append.  Host
+    arrays, uploaded by the caller."""
     nb, hkv = w.num_blocks, w.num_kv_heads
+    rng = np.random.default_rng(seed)
+    ks, vs = [], []
+    for _ in range(LAYERS):
+        kb = W.randn_bf16(rng, (nb, hkv, 16, 128))
+        vb = W.randn_bf16(rng, (nb, hkv, 16, 128))
+        if fmt == pkv.KV_BF16:
+            ks.append(kb)
+            vs.append(vb)
+            continue
+        tok = lambda p: np.ascontiguousarray(p.transpose(0, 2, 1, 3).reshape(nb * 16, hkv, 128))
+        slots = np.arange(nb * 16, dtype=np.int64)
+        if fmt == pkv.KV_Q8_0:
+            kq = np.zeros((nb, hkv, oracle.Q8_TILE_BYTES), np.uint8)
+            vq = np.zeros_like(kq)
+            oracle.kv_append_q8_0(kq, vq, slots, tok(kb), tok(vb))
+        else:
+            kq = np.zeros((nb, hkv, 16, 128), np.uint8)
+            vq = np.zeros_like(kq)
+            oracle.kv_append_fp8(kq, vq, slots, tok(kb), tok(vb))
+        ks.append(kq)
+        vs.append(vq)
+    return np.stack(ks), np.stack(vs)
+
+
+def _upload_pools(fmt, kh, vh):
     if fmt == pkv.KV_BF16:
-        k = torch.empty((LAYERS, nb, hkv, 16, 128), dtype=torch.bfloat16, device="cuda")
-        v = torch.empty_like(k)
-        for l in range(LAYERS):
-            W.fill_pool_device(k[l], seed + 2 * l)
-            W.fill_pool_device(v[l], seed + 2 * l + 1)
-        return k, v
-    tile = (pkv.Q8_TILE_BYTES,) if fmt == pkv.KV_Q8_0 else (16, 128)
-    k = torch.empty((LAYERS, nb, hkv) + tile, dtype=torch.uint8, device="cuda")
-    v = torch.empty_like(k)
-    tmp_k = torch.empty((nb, hkv, 16, 128), dtype=torch.bfloat16, device="cuda")
-    tmp_v = torch.empty_like(tmp_k)
-    slots = torch.arange(nb * 16, dtype=torch.int64, device="cuda")
-    tok = lambda p: p.permute(0, 2, 1, 3).contiguous().view(nb * 16, hkv, 128)
-    append = pkv.kv_append_q8_0 if fmt == pkv.KV_Q8_0 else pkv.kv_append_fp8_e4m3
+        return _dev_bf16(kh), _dev_bf16(vh)
+    return torch.from_numpy(kh).cuda(), torch.from_numpy(vh).cuda()
+
+
+def _oracle_step(fmt, kh, vh, host, w):
+    """The step on the host with the oracle: per layer the append, then the
+    attention (FP64; over the stored values for the quantised formats).
+    Updates the host pools in place; returns float64 [LAYERS][B][q_len][Hq][D]."""
+    outs = []
     for l in range(LAYERS):
-        W.fill_pool_device(tmp_k, seed + 2 * l)
-        W.fill_pool_device(tmp_v, seed + 2 * l + 1)
-        append(k[l], v[l], slots, tok(tmp_k), tok(tmp_v))
-    return k, v
+        if fmt == pkv.KV_BF16:
+            oracle.kv_append(kh[l], vh[l], w.slot_mapping, host["k_new"][l], host["v_new"][l])
+            outs.append(oracle.paged_attention(host["q"][l], kh[l], vh[l], w.block_tables, w.context_lens, w.q_len,
+                                               w.scale))
+            continue
+        if fmt == pkv.KV_Q8_0:
+            oracle.kv_append_q8_0(kh[l], vh[l], w.slot_mapping, host["k_new"][l], host["v_new"][l])
+            kd, vd = oracle.dequantize_q8_0(kh[l]), oracle.dequantize_q8_0(vh[l])
+        else:
+            oracle.kv_append_fp8(kh[l], vh[l], w.slot_mapping, host["k_new"][l], host["v_new"][l])
+            kd, vd = oracle.dequantize_fp8(kh[l]), oracle.dequantize_fp8(vh[l])
+        outs.append(oracle.paged_attention_f64(host["q"][l], kd, vd, w.block_tables, w.context_lens, w.q_len,
+                                               w.scale))
+    return np.stack(outs)
 
 
 def _direct_step(fmt, kp, vp, st, w, bps, ws, cascade):
@@ -112,7 +156,7 @@ CASES = {
 
 
 @pytest.mark.parametrize("case", list(CASES))
-def test_graph_equals_direct_calls_on_both_buffer_sets(case):
+def test_graph_equals_direct_calls_and_oracle_on_both_buffer_sets(case):
     c = CASES[case]
     fmt, ql = c["fmt"], c.get("q_len", 1)
     ctx = np.asarray(c["ctx"]) + (ql if ql > 1 else 0)
@@ -139,8 +183,10 @@ def test_graph_equals_direct_calls_on_both_buffer_sets(case):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
 
     rng = np.random.default_rng(77)
-    sets = [_buffer_set(w, rng, casc_arrays) for _ in range(2)]
-    kp, vp = _pools(fmt, w, seed=900)
+    sets, hosts = zip(*[_buffer_set(w, rng, casc_arrays) for _ in range(2)])
+    sets = list(sets)
+    kh, vh = _host_pools(fmt, w, seed=900)
+    kp, vp = _upload_pools(fmt, kh, vh)
     kp_d, vp_d = kp.clone(), vp.clone()
     desc = pkv.CacheDesc(w.num_blocks, 16, w.num_kv_heads, 128)
     g = pkv.DecodeGraph(list(kp), list(vp), desc, sets, num_seqs=b, q_len=ql, num_q_heads=hq,
@@ -160,3 +206,17 @@ def test_graph_equals_direct_calls_on_both_buffer_sets(case):
         assert torch.equal(got, ref), f"{case}: buffer set {s} differs from the direct calls"
         assert torch.isfinite(sets[s]["out"].float()).all()
     assert torch.equal(kp, kp_d) and torch.equal(vp, vp_d), f"{case}: pools differ after the appends"
+
+    # the same three steps on the host with the oracle
+    expect = {}
+    for s in (0, 1, 0):
+        expect[s] = _oracle_step(fmt, kh, vh, hosts[s], w)
+    for s in (0, 1):
+        got = sets[s]["out"].float().cpu().numpy().astype(np.float64)
+        for l in range(LAYERS):
+            assert_close(got[l], expect[s][l], what=f"{case}: buffer set {s}, layer {l} vs oracle")
+    if fmt == pkv.KV_BF16:
+        kg, vg = kp.view(torch.int16).cpu().numpy().view(np.uint16), vp.view(torch.int16).cpu().numpy().view(np.uint16)
+    else:
+        kg, vg = kp.cpu().numpy(), vp.cpu().numpy()
+    assert np.array_equal(kg, kh) and np.array_equal(vg, vh), f"{case}: pools differ from the oracle's appends"
