@@ -221,10 +221,14 @@ pkv_status pkv_paged_attention_cascade(void* out, const void* q, const void* k_c
  * the row it read.  That requires token r to be request r's new token and
  * slot_mapping[r] to be the slot the block table gives that position (or
  * negative: not stored); any other slot is stored as pkv_kv_append would but
- * sets PKV_DEVERR_SLOT, and the attention result is then undefined.  Other
- * shapes issue the append, then the attention.  Results equal the two calls'
- * bit for bit.  Host-detectable errors of either call return before
- * anything is enqueued.
+ * sets PKV_DEVERR_SLOT, and the attention result is then undefined.  A token
+ * is stored only when its row has a position context_lens[r] - 1 inside the
+ * block table: a slot >= 0 for a row with context_lens[r] <= 0 is a caller
+ * error (the token is not stored; PKV_DEVERR_SLOT), and a context longer than
+ * the table (PKV_DEVERR_CONTEXT) leaves its token unstored too.  Other
+ * shapes issue the append, then the attention.  For inputs that set no device
+ * error, results equal the two calls' bit for bit.  Host-detectable errors of
+ * either call return before anything is enqueued.
  */
 pkv_status pkv_paged_attention_append(void* out, const void* q, void* k_cache, void* v_cache,
                                       const pkv_cache_desc* cache, const int32_t* block_tables,
@@ -241,7 +245,8 @@ pkv_status pkv_paged_attention_append(void* out, const void* q, void* k_cache, v
  * launch does; other counts issue the append, then the cascade.  A new token
  * must lie past its request's shared prefix (never append into a block
  * another table references); one inside it is not stored and sets
- * PKV_DEVERR_SLOT.  Results equal the two calls' bit for bit otherwise.
+ * PKV_DEVERR_SLOT, as does a slot >= 0 for a row with context_lens[r] <= 0.
+ * Results equal the two calls' bit for bit otherwise.
  */
 pkv_status pkv_paged_attention_cascade_append(
     void* out, const void* q, void* k_cache, void* v_cache, const pkv_cache_desc* cache, const int32_t* block_tables,
@@ -271,7 +276,10 @@ pkv_status pkv_paged_attention_cascade_append(
  *     routine.  The caller still provides inputs and outputs.
  *   - The first call on a device looks the array's device address up
  *     (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  Host threads may make first calls concurrently (the
+ *     lookup is serialised).  cudaDeviceReset on a device invalidates the
+ *     cached address: do not call this entry point on that device again in
+ *     the same process.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents.  Nothing in it must start at zero.  Calls that can overlap on
  *     the GPU (unordered streams) race on it: order them.
@@ -313,6 +321,26 @@ pkv_status pkv_attn_combine(void* out, float* out_lse, const float* partial_o,
  * *host_word; when reset != 0, clear it.  Synchronises the device.
  */
 pkv_status pkv_get_device_error(uint32_t* host_word, int32_t reset);
+
+/*
+ * pkv_selftest_bounded_wait -- exercise the fail-fast path of the kernels'
+ * pipeline waits.  Every wait in libpkv gives up after a wall-time limit and
+ * sets PKV_DEVERR_TIMEOUT rather than hang (the PhyAI deployment page
+ * "Parallel serving", failure handling: fail fast, a step that cannot finish
+ * within its timeout is reported, not waited on).  Healthy calls never reach
+ * the limit, so this entry point launches a
+ * one-CTA kernel whose consumer waits, with the same bounded wait, on a ring
+ * stage 0 that its producer arms and a stage 1 that it arms only when
+ * arm_all != 0.
+ *   wait_limit_us : 1 .. 1,000,000 (else PKV_ERR_SHAPE): the limit of each
+ *                   wait, in microseconds of GPU wall time.
+ *   arm_all       : 0 = stage 1 is never armed: its wait runs out and the
+ *                   error word gets PKV_DEVERR_TIMEOUT; != 0 = both waits
+ *                   complete and nothing is reported.
+ * The kernel issues no memory copy and returns normally either way; the
+ * stream and context stay usable.  Stream-ordered, allocates nothing.
+ */
+pkv_status pkv_selftest_bounded_wait(uint32_t wait_limit_us, int32_t arm_all, void* stream);
 
 /*
  * Block pool and copy-on-write -- the host-side bookkeeping of §8.3.1/§8.3.2
@@ -481,8 +509,10 @@ pkv_status pkv_paged_attention_fp8_e4m3(void* out, const void* q, const void* k_
  * and uses them in place of the rows it read, as pkv_paged_attention_append
  * does; other counts issue the append, then the attention.  A slot other than
  * the one the block table gives that position is stored as the append would
- * but sets PKV_DEVERR_SLOT (the result is then undefined).  Results equal the
- * two calls' bit for bit otherwise.
+ * but sets PKV_DEVERR_SLOT (the result is then undefined); rows with
+ * context_lens[r] <= 0 or longer than the table store nothing, as for
+ * pkv_paged_attention_append.  Results equal the two calls' bit for bit
+ * otherwise.
  */
 pkv_status pkv_paged_attention_fp8_e4m3_append(void* out, const void* q, void* k_cache, void* v_cache,
                                                const pkv_cache_desc* cache, const int32_t* block_tables,

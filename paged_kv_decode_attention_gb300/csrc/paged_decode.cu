@@ -217,6 +217,12 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
       // other requests read is not allowed; it is not stored
       report(a.err, PKV_DEVERR_SLOT);
     }
+  } else if (a.k_new != nullptr && ctx <= 0 && split == 0 && kvh == 0 && threadIdx.x == 0 &&
+             a.slot_mapping[r] >= 0) {
+    // a stored token needs a position ctx - 1 >= 0: a slot for an empty row is
+    // a caller error and the token is not stored (a context beyond the table
+    // is reported above as PKV_DEVERR_CONTEXT and its token not stored either)
+    report(a.err, PKV_DEVERR_SLOT);
   }
 
   const bool has_prefix = a.prefix_o != nullptr && start > 0;

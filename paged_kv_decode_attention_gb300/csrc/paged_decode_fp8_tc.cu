@@ -535,6 +535,11 @@ __global__ void __launch_bounds__(kFtThreads, 1)
       const int64_t orow0 = static_cast<int64_t>(x.r) * hq + x.kvh * kGroup;
       if (threadIdx.x == 128 && x.split == 0 && x.kvh == 0 && x.ctx_raw > a.max_blocks * kBlockSize)
         report(a.err, PKV_DEVERR_CONTEXT);
+      // fused append: a slot for an empty row has no position ctx - 1 to go
+      // to; the token is not stored and the caller's error is reported
+      if (kFused && threadIdx.x == 128 && x.split == 0 && x.kvh == 0 && x.ctx_raw <= 0 &&
+          a.slot_mapping[x.r] >= 0)
+        report(a.err, PKV_DEVERR_SLOT);
       if (x.n_tiles == 0) {  // padding row or a split past the context
         if (direct)
           reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow0 * kHeadDim)[t] = make_uint2(0, 0);

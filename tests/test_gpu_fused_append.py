@@ -205,15 +205,47 @@ def test_fused_random_shapes(seed):
     _assert_same(_both(w, bps), f"random seed={seed} b={b} bps={bps}")
 
 
-def _fp8_pools(d, w):
-    """E4M3 pools holding the workload's BF16 cache, stored through the E4M3 append."""
-    nb, hkv = w.num_blocks, w.num_kv_heads
-    tok = lambda t: t.permute(0, 2, 1, 3).contiguous().view(nb * 16, hkv, 128)
-    kq = torch.empty((nb, hkv, 16, 128), dtype=torch.uint8, device="cuda")
-    vq = torch.empty_like(kq)
-    pkv.kv_append_fp8_e4m3(kq, vq, torch.arange(nb * 16, dtype=torch.int64, device="cuda"), tok(d["k_cache"]),
-                           tok(d["v_cache"]))
+def _tokens_of_pool(pool: np.ndarray) -> np.ndarray:
+    nb, hkv, bs, d = pool.shape
+    return np.ascontiguousarray(pool.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
+
+
+def _fp8_host_pools(k_pool: np.ndarray, v_pool: np.ndarray):
+    """E4M3 pools holding BF16 host pools, stored by the oracle's append."""
+    nb, hkv = k_pool.shape[:2]
+    kq = np.zeros((nb, hkv, 16, 128), np.uint8)
+    vq = np.zeros_like(kq)
+    oracle.kv_append_fp8(kq, vq, np.arange(nb * 16, dtype=np.int64), _tokens_of_pool(k_pool),
+                         _tokens_of_pool(v_pool))
     return kq, vq
+
+
+def _fp8_pools(d, w):
+    """Device E4M3 pools holding the workload's BF16 cache (the oracle's rounding)."""
+    kq, vq = _fp8_host_pools(w.k_cache, w.v_cache)
+    return torch.from_numpy(kq).cuda(), torch.from_numpy(vq).cuda()
+
+
+def _fp8_oracle(w, kq: np.ndarray, vq: np.ndarray, q=None, tables=None, ctx=None, slots=None, k_new=None,
+                v_new=None):
+    """The step with the oracle on copies of host E4M3 pools: the rounding
+    append of the new tokens, then FP64 attention over the stored values."""
+    kq, vq = kq.copy(), vq.copy()
+    oracle.kv_append_fp8(kq, vq, w.slot_mapping if slots is None else slots, w.k_new if k_new is None else k_new,
+                         w.v_new if v_new is None else v_new)
+    out = oracle.paged_attention_f64(w.q if q is None else q, oracle.dequantize_fp8(kq), oracle.dequantize_fp8(vq),
+                                     w.block_tables if tables is None else tables,
+                                     w.context_lens if ctx is None else ctx, 1, w.scale)
+    return out, kq, vq
+
+
+def _assert_fp8_oracle(res, w, what):
+    """The fused call's output and pools against the oracle's step."""
+    out, kf, vf = res[0]
+    ref, kq, vq = _fp8_oracle(w, *_fp8_host_pools(w.k_cache, w.v_cache))
+    assert np.array_equal(kf.cpu().numpy(), kq) and np.array_equal(vf.cpu().numpy(), vq), \
+        f"{what}: E4M3 pools differ from the oracle's append"
+    assert_close(bf16_to_f64(out), ref, what=f"{what} vs oracle")
 
 
 def _fp8_both(w, bps=0):
@@ -257,7 +289,10 @@ def test_fused_fp8_equals_append_then_attention(bps):
     ctx = np.asarray(RAGGED_FP8)
     need = int(sum(-(-int(c) // 16) for c in ctx))
     w = W.build("fused-fp8", ctx, need + 30, seed=71)
-    _assert_same_fp8(_fp8_both(w, bps), f"fused fp8 bps={bps}")
+    res = _fp8_both(w, bps)
+    _assert_same_fp8(res, f"fused fp8 bps={bps}")
+    assert not res[0][0][ctx == 0].float().abs().sum()
+    _assert_fp8_oracle(res, w, f"fused fp8 bps={bps}")
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -271,7 +306,9 @@ def test_fused_fp8_random_shapes(seed):
     w.slot_mapping = w.slot_mapping.copy()
     w.slot_mapping[rng.random(b) < 0.1] = -1
     bps = int(rng.choice([0, 0, 5, 16, 40, 1000]))
-    _assert_same_fp8(_fp8_both(w, bps), f"fp8 random seed={seed} b={b} bps={bps}")
+    res = _fp8_both(w, bps)
+    _assert_same_fp8(res, f"fp8 random seed={seed} b={b} bps={bps}")
+    _assert_fp8_oracle(res, w, f"fp8 random seed={seed} b={b} bps={bps}")
 
 
 def test_fused_fp8_wrong_slot_sets_the_error_word():
@@ -314,7 +351,6 @@ def test_fused_fp8_short_chat_full_size():
     kq = torch.empty((nb, hkv, 16, 128), dtype=torch.uint8, device="cuda")
     vq = torch.empty_like(kq)
     pkv.kv_append_fp8_e4m3(kq, vq, torch.arange(nb * 16, dtype=torch.int64, device="cuda"), tok(kb), tok(vb))
-    del kb, vb
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     q, kn, vn = (dev(x).view(torch.bfloat16) for x in (w.q, w.k_new, w.v_new))
     tables, ctx, slots = dev(w.block_tables), dev(w.context_lens), dev(w.slot_mapping)
@@ -332,6 +368,36 @@ def test_fused_fp8_short_chat_full_size():
     assert torch.equal(out_f.view(torch.int16), out_s.view(torch.int16)), "full-size fp8: outputs differ"
     assert torch.equal(kf, kq) and torch.equal(vf, vq), "full-size fp8: pools differ"
     assert torch.isfinite(out_f.float()).all()
+    _sampled_oracle_check(w, kb, vb, out_f, kf, vf, fp8=True)
+
+
+def _sampled_oracle_check(w, kb, vb, out, kpool, vpool, fp8):
+    """Requests 0, 17 and 36 of a full-size batch against the oracle: their
+    blocks of the device-filled BF16 pools (E4M3-rounded by the oracle for
+    fp8) plus the new token appended by the oracle, compared with the blocks
+    the fused call left (bit for bit) and with its output."""
+    got = bf16_to_f64(out)
+    for r in [0, 17, 36]:
+        n = -(-int(w.context_lens[r]) // 16)
+        idx = torch.from_numpy(w.block_tables[r, :n].astype(np.int64)).cuda()
+        sub = lambda p: p.index_select(0, idx).cpu().view(torch.int16).numpy().view(np.uint16)
+        kh, vh = sub(kb), sub(vb)
+        slot = int(w.slot_mapping[r])
+        assert slot // 16 == int(w.block_tables[r, n - 1])
+        sub_slot = np.array([(n - 1) * 16 + slot % 16], np.int64)
+        table = np.arange(n, dtype=np.int32)[None, :]
+        if fp8:
+            ref, kq_ref, vq_ref = _fp8_oracle(w, *_fp8_host_pools(kh, vh), q=w.q[r:r + 1], tables=table,
+                                              ctx=w.context_lens[r:r + 1], slots=sub_slot,
+                                              k_new=w.k_new[r:r + 1], v_new=w.v_new[r:r + 1])
+            k_got, v_got = kpool.index_select(0, idx).cpu().numpy(), vpool.index_select(0, idx).cpu().numpy()
+        else:
+            kq_ref, vq_ref = kh.copy(), vh.copy()
+            oracle.kv_append(kq_ref, vq_ref, sub_slot, w.k_new[r:r + 1], w.v_new[r:r + 1])
+            ref = oracle.paged_attention(w.q[r:r + 1], kq_ref, vq_ref, table, w.context_lens[r:r + 1], 1, w.scale)
+            k_got, v_got = sub(kpool), sub(vpool)
+        assert np.array_equal(k_got, kq_ref) and np.array_equal(v_got, vq_ref), f"request {r}: pool bytes"
+        assert_close(got[r:r + 1], ref, what=f"full-size fused request {r} vs oracle")
 
 
 def test_fused_bf16_short_chat_full_size():
@@ -345,6 +411,7 @@ def test_fused_bf16_short_chat_full_size():
     vc = torch.empty_like(kc)
     W.fill_pool_device(kc, seed=23)
     W.fill_pool_device(vc, seed=24)
+    kb0, vb0 = kc.clone(), vc.clone()  # the pools before the step, for the oracle
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     q, kn, vn = (dev(x).view(torch.bfloat16) for x in (w.q, w.k_new, w.v_new))
     tables, ctx, slots = dev(w.block_tables), dev(w.context_lens), dev(w.slot_mapping)
@@ -363,3 +430,52 @@ def test_fused_bf16_short_chat_full_size():
     assert torch.equal(kf.view(torch.int16), kc.view(torch.int16)) and \
         torch.equal(vf.view(torch.int16), vc.view(torch.int16)), "full-size bf16: pools differ"
     assert torch.isfinite(out_f.float()).all()
+    _sampled_oracle_check(w, kb0, vb0, out_f, kf, vf, fp8=False)
+
+
+def _empty_row_with_slot(fp8):
+    """Request 1 has context 0 but a slot >= 0 (a spare block of the pool):
+    the fused call stores nothing there and reports PKV_DEVERR_SLOT; the other
+    rows are unaffected."""
+    ctx = np.asarray([100, 0, 300])
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("empty-row-slot", ctx, need + 30, seed=67)
+    used = set()
+    for r, c in enumerate(ctx):
+        used.update(int(b) for b in w.block_tables[r, :-(-int(c) // 16)])
+    spare = next(b for b in range(w.num_blocks) if b not in used)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[1] = spare * 16 + 7
+    d = to_device(w)
+    out = torch.full_like(d["q"], float("nan"))
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    if fp8:
+        kc, vc = _fp8_pools(d, w)
+        k0, v0 = kc.clone(), vc.clone()
+        pkv.paged_attention_fp8_e4m3_append(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
+                                            d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=1000,
+                                            workspace=ws)
+    else:
+        kc, vc = d["k_cache"], d["v_cache"]
+        k0, v0 = kc.clone(), vc.clone()
+        pkv.paged_attention_append(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], 1, w.scale,
+                                   d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=1000,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(reset=True) == pkv.DEVERR_SLOT
+    assert torch.equal(kc[spare], k0[spare]) and torch.equal(vc[spare], v0[spare]), "token stored for an empty row"
+    assert not out[1].float().abs().sum(), "empty row must output zeros"
+    w.slot_mapping[1] = -1  # what the other rows must see: the step without request 1's token
+    if fp8:
+        ref = _fp8_oracle(w, *_fp8_host_pools(w.k_cache, w.v_cache))[0]
+    else:
+        ref = oracle.run_workload(w)
+    assert_close(bf16_to_f64(out), ref, what="rows beside an empty row with a slot")
+
+
+def test_fused_empty_row_with_a_slot_stores_nothing_and_sets_the_error_word():
+    _empty_row_with_slot(fp8=False)
+
+
+def test_fused_fp8_empty_row_with_a_slot_stores_nothing_and_sets_the_error_word():
+    _empty_row_with_slot(fp8=True)
