@@ -4,6 +4,7 @@
 // carving and stream-ordered launches.  Nothing here allocates, frees or
 // synchronises device memory (except pkv_get_device_error, which reads the
 // error word and documents that it synchronises).
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -20,8 +21,10 @@ namespace {
 __device__ unsigned int g_device_error;
 
 constexpr int kMaxDevices = 64;
-unsigned int* g_error_ptr[kMaxDevices];
-int g_sm_count[kMaxDevices];
+// Per-device caches, filled on first use.  Host threads may race on a first
+// use: each computes the same value and the stores are atomic.
+std::atomic<unsigned int*> g_error_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
 
 }  // namespace
 
@@ -30,12 +33,14 @@ int g_sm_count[kMaxDevices];
 unsigned int* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (g_error_ptr[dev] == nullptr) {
+  unsigned int* w = g_error_ptr[dev].load(std::memory_order_acquire);
+  if (w == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    g_error_ptr[dev] = static_cast<unsigned int*>(p);
+    w = static_cast<unsigned int*>(p);
+    g_error_ptr[dev].store(w, std::memory_order_release);
   }
-  return g_error_ptr[dev];
+  return w;
 }
 
 namespace {
@@ -48,12 +53,12 @@ constexpr int kGb300Sms = 152;
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kGb300Sms;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kGb300Sms;
-    g_sm_count[dev] = n;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 pkv_status check_cache(const pkv_cache_desc* c) {

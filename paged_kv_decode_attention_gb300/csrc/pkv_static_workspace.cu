@@ -15,11 +15,17 @@
 // host-side stand-in, so the device address is looked up once per device with
 // cudaGetSymbolAddress, with that device current, and cached.  That happens on
 // the first call made on a device, so that first call should come before any
-// stream capture.  All calls on a device share the one array: calls that may
+// stream capture.  The cache is per device and safe for concurrent first calls
+// from several host threads; a cudaDeviceReset of a device leaves its cached
+// address stale, so this entry point is not for use on that device after a
+// reset.  All calls on a device share the one array: calls that may
 // overlap on the GPU (different streams without ordering between them) race
 // on it.  Nothing in it needs to start at zero, because each call writes every
 // partial log-sum-exp it later reads and only reads partial outputs it wrote.
+#include <atomic>
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "pkv.h"
@@ -29,25 +35,31 @@ namespace {
 static __device__ __align__(256) uint8_t g_static_workspace[PKV_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_static_workspace_ptr[kMaxDevices];
+std::atomic<void*> g_static_workspace_ptr[kMaxDevices];
+std::mutex g_static_workspace_lookup;
 
-// Device address of this device's copy of the array (looked up once per device).
+// Device address of this device's copy of the array (looked up once per
+// device; a first call racing another thread's waits for its lookup).
 void* static_workspace_address(pkv_status* st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     *st = PKV_ERR_CUDA;
     return nullptr;
   }
-  if (g_static_workspace_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) {
-      *st = PKV_ERR_CUDA;
-      return nullptr;
+  void* p = g_static_workspace_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_static_workspace_lookup);
+    p = g_static_workspace_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) {
+        *st = PKV_ERR_CUDA;
+        return nullptr;
+      }
+      g_static_workspace_ptr[dev].store(p, std::memory_order_release);
     }
-    g_static_workspace_ptr[dev] = p;
   }
   *st = PKV_OK;
-  return g_static_workspace_ptr[dev];
+  return p;
 }
 
 }  // namespace

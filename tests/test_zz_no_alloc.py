@@ -2,15 +2,22 @@
 callers that cannot allocate device memory (code inside a memory manager or
 an allocation hook, frameworks that forbid allocation on the hot path, plain
 C callers without a CUDA allocator).  It keeps split-KV partials in a scratch
-array compiled into the library.  Checked here through the C ABI against the
-ordinary entry point (which takes a caller workspace) on two calls in a row,
-so the second call runs on scratch that still holds the first call's data."""
+array compiled into the library.
+
+Checked here through the C ABI on three calls in a row, each split into more
+than 8 ranges so that its partials really go through the array (fewer ranges
+merge on chip and leave it untouched).  The second call has the first call's
+shape but other context lengths, so rows that now have fewer ranges sit next
+to stale partials of the first call; the third has another shape.  Every call
+is compared with the ordinary entry point (which takes a caller workspace)
+and with the FP64 oracle."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from gpu_util import assert_close, bf16_to_f64, to_device
 
@@ -37,8 +44,6 @@ def _call_static(pkv, f, w, d, out, bps):
 
 
 def _reference(pkv, w, d, bps):
-    if bps == 0:
-        bps = pkv.choose_kv_blocks_per_split(w.num_seqs, w.num_kv_heads, w.q_len, w.max_blocks_per_seq)
     ws_bytes = pkv.workspace_size(w.num_seqs, w.q_len, w.num_q_heads, w.max_blocks_per_seq, bps)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(d["q"])
@@ -47,13 +52,17 @@ def _reference(pkv, w, d, bps):
     return out
 
 
-def test_static_workspace_entry_matches_workspace_entry_on_consecutive_calls():
+def test_static_workspace_entry_matches_workspace_entry_and_oracle_on_consecutive_calls():
     pkv, f = _static_entry()
     cases = [
-        (W.build("first", [2300, 17, 700, 1, 0, 4100], 800, seed=21), 8),
-        (W.build("second", [5, 300, 64, 1999], 400, q_len=3, seed=22), 0),
+        (W.build("first", [2300, 17, 700, 1, 0, 4100], 800, seed=21, max_blocks=257), 8),
+        (W.build("second", [40, 4000, 1, 0, 2000, 300], 800, seed=24, max_blocks=257), 8),
+        (W.build("third", [5, 300, 64, 1999], 400, q_len=3, seed=22), 10),
     ]
     for w, bps in cases:
+        # more than 8 ranges: the partials go through the scratch array
+        assert -(-w.max_blocks_per_seq // bps) > 8
+        assert pkv.workspace_size(w.num_seqs, w.q_len, w.num_q_heads, w.max_blocks_per_seq, bps) > 0
         d = to_device(w)
         pkv.kv_append(d["k_cache"], d["v_cache"], d["slot_mapping"], d["k_new"], d["v_new"])
         out = torch.full_like(d["q"], float("nan"))
@@ -61,7 +70,10 @@ def test_static_workspace_entry_matches_workspace_entry_on_consecutive_calls():
         assert st == 0, pkv.lib().pkv_status_string(st)
         ref = _reference(pkv, w, d, bps)
         torch.cuda.synchronize()
-        assert_close(bf16_to_f64(out), bf16_to_f64(ref), what=f"static workspace, {w.name}")
+        got = bf16_to_f64(out)
+        assert_close(got, bf16_to_f64(ref), what=f"static workspace vs workspace entry, {w.name}")
+        assert_close(got, oracle.run_workload(w), what=f"static workspace vs oracle, {w.name}")
+        assert not got[w.context_lens == 0].any(), f"{w.name}: padding rows must be zero"
     assert pkv.get_device_error(reset=True) == 0
 
 
