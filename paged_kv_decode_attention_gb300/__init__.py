@@ -27,7 +27,7 @@ __all__ = [
     "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "Q8_TILE_BYTES", "kv_append_q8_0", "paged_attention_q8_0",
     "choose_kv_blocks_per_split_q8_0", "choose_kv_blocks_per_split_fp8_e4m3", "workspace_size_q8_0", "copy_blocks_q8_0", "FP8_TILE_BYTES",
     "kv_append_fp8_e4m3", "paged_attention_fp8_e4m3", "paged_attention_fp8_e4m3_append", "copy_blocks_fp8_e4m3",
-    "DecodeGraph", "KV_BF16", "KV_Q8_0", "KV_FP8_E4M3",
+    "DecodeGraph", "KV_BF16", "KV_Q8_0", "KV_FP8_E4M3", "selftest_bounded_wait",
 ]
 
 DEVERR_BLOCK_ID = 1
@@ -149,6 +149,8 @@ def _load():
     lib.pkv_decode_graph_destroy.restype = None
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.pkv_get_device_error.restype = ctypes.c_int
+    lib.pkv_selftest_bounded_wait.argtypes = [ctypes.c_uint32, i32, p]
+    lib.pkv_selftest_bounded_wait.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
     del i64
@@ -730,3 +732,11 @@ def get_device_error(reset: bool = True) -> int:
     word = ctypes.c_uint32(0)
     _check(_lib.pkv_get_device_error(ctypes.byref(word), 1 if reset else 0), "pkv_get_device_error")
     return int(word.value)
+
+
+def selftest_bounded_wait(wait_limit_us: int, arm_all: bool = False, stream=None) -> None:
+    """Run the kernels' bounded wait on a barrier that nothing arms (or, with
+    arm_all, on armed ones): with nothing arming it the wait gives up after
+    wait_limit_us and sets DEVERR_TIMEOUT; read it with get_device_error."""
+    _check(_lib.pkv_selftest_bounded_wait(int(wait_limit_us), 1 if arm_all else 0, _stream_ptr(stream)),
+           "pkv_selftest_bounded_wait")

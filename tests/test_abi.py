@@ -252,3 +252,9 @@ def test_paged_attention_fp8_e4m3_append_argument_errors():
     # the attention's own checks run before anything is enqueued: no query
     assert f(None, None, 4096, 4096, ctypes.byref(d), 4096, 1, 4096, 1, 32, 1.0, 0, None, 0, 4096, 4096, 4096, 1,
              None) == 1
+
+
+def test_selftest_bounded_wait_rejects_limits_outside_its_range():
+    lib = pkv.lib()
+    assert lib.pkv_selftest_bounded_wait(0, 0, None) == 2
+    assert lib.pkv_selftest_bounded_wait(1000001, 0, None) == 2
