@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import gc
 import json
 import math
 import os
@@ -222,7 +223,8 @@ def oracle_sample_q8(w, kq_dev, vq_dev, max_seqs: int):
     return sub, kq, vq
 
 
-def time_oracle_q8(sub, kq, vq, budget_s: float = 12.0, max_reps: int = 200, kv: str = "q8_0"):
+def time_oracle_q8(sub, kq, vq, budget_s: float = 12.0, max_reps: int = 200, kv: str = "q8_0",
+                   num_threads: int = 0):
     """The oracle's quantising append, dequantisation and FP64 attention on the sample."""
     import oracle
     attn_b, app_b = bytes_per_layer(sub, kv)
@@ -231,32 +233,34 @@ def time_oracle_q8(sub, kq, vq, budget_s: float = 12.0, max_reps: int = 200, kv:
     reps, t0 = 0, time.perf_counter()
     while True:
         append(kq, vq, sub.slot_mapping, sub.k_new, sub.v_new)
-        oracle.paged_attention_f64(sub.q, deq(kq), deq(vq), sub.block_tables, sub.context_lens, 1, sub.scale)
+        oracle.paged_attention_f64(sub.q, deq(kq), deq(vq), sub.block_tables, sub.context_lens, 1, sub.scale,
+                                   num_threads=num_threads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= max_reps:
             break
     per = el / reps
     return {"gbs": (attn_b + app_b) / per / 1e9, "s_per_layer_call": per, "reps": reps,
-            "cores": oracle.max_threads(), "seqs": sub.num_seqs}
+            "cores": num_threads or oracle.max_threads(), "seqs": sub.num_seqs}
 
 
-def time_oracle(sub, budget_s: float = 12.0, max_reps: int = 200):
-    """Run the oracle's append + attention on the sample until ~budget_s; GB/s of algorithmic bytes."""
+def time_oracle(sub, budget_s: float = 12.0, max_reps: int = 200, num_threads: int = 0):
+    """Run the oracle's append + attention on the sample until ~budget_s; GB/s
+    of algorithmic bytes.  num_threads 0 = all host cores."""
     import oracle
     attn_b, app_b = bytes_per_layer(sub)
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.kv_append(sub.k_cache, sub.v_cache, sub.slot_mapping, sub.k_new, sub.v_new)
         oracle.paged_attention(sub.q, sub.k_cache, sub.v_cache, sub.block_tables, sub.context_lens, sub.q_len,
-                               sub.scale)
+                               sub.scale, num_threads=num_threads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= max_reps:
             break
     per = el / reps
     return {"gbs": (attn_b + app_b) / per / 1e9, "s_per_layer_call": per, "reps": reps,
-            "cores": oracle.max_threads(), "seqs": sub.num_seqs}
+            "cores": num_threads or oracle.max_threads(), "seqs": sub.num_seqs}
 
 
 # ---------------------------------------------------------------------------
@@ -283,6 +287,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--oracle-budget-s", type=float, default=12.0)
+    ap.add_argument("--kernel-pass-s", type=float, default=1.0,
+                    help="GPU seconds of the sustained kernel-timing pass (at least --steps replays)")
+    ap.add_argument("--per-config", action=argparse.BooleanOptionalAction, default=True,
+                    help="default short-chat run: also time the long, mixed and chunk workloads")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--num-seqs", type=int, default=0, help="chunk workload: fewer requests (small profiling cases)")
     ap.add_argument("--sweep", action="store_true", help="q_len-1 batch x context sweep instead of a step benchmark")
@@ -295,8 +303,51 @@ def main():
     if args.sweep:
         return run_sweep(args)
     world, rank, local = dist_init(args.gpus)
-    w, layers = make_workload(args.workload, args.seed, args.num_seqs)
-    if args.layers > 0:
+    if args.impl == "reference":
+        w, layers = make_workload(args.workload, args.seed, args.num_seqs)
+        if args.layers > 0:
+            layers = args.layers
+        attn_b, app_b = bytes_per_layer(w, args.kv)
+        return run_reference(args, world, rank, w, layers, layers * (attn_b + app_b))
+    line = bench_one(args, args.workload, world, rank, local, headline=True)
+    # the other decode targets in the same run (the default run only): the
+    # long shared-prefix batch, the mixed batch and the streaming chunks,
+    # each with its own timing, roofline and clocks
+    if args.per_config and args.workload == "short" and args.kv == "bf16" and args.layers == 0:
+        per = {}
+        for name in PER_CONFIG:
+            gc.collect()  # the previous workload's pools
+            torch.cuda.empty_cache()
+            r = bench_one(args, name, world, rank, local, headline=False)
+            if r is not None:
+                per[name] = {k: r[k] for k in ("ms_per_step", "us_per_layer_call", "us_per_layer_call_isolated",
+                                               "value", "bytes_per_step", "attention_tokens_layers_per_s",
+                                               "decode_steps_per_s", "roofline", "clocks", "clocks_kernel_pass",
+                                               "launch")}
+                per[name]["workload"] = r["config"]["workload"]
+                per[name]["unit"] = "GB/s"
+        if line is not None:
+            line["per_config"] = per
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+# the other configurations the default run measures beside the headline
+PER_CONFIG = ("long", "mixed", "chunk")
+
+
+def l2_text(w, layers: int, kv: str) -> str:
+    """How the timed loop keeps KV out of L2 (the same text for both arms)."""
+    tile = {"q8_0": 2176, "fp8_e4m3": 2048}.get(kv, 4096)
+    return "inputs larger than L2: one KV pool per layer, %.1f GB total" % (
+        2 * layers * w.num_blocks * W.NUM_KV_HEADS * tile / 1e9)
+
+
+def bench_one(args, name: str, world: int, rank: int, local: int, headline: bool):
+    """Benchmark one workload; returns the JSON line's dict on rank 0 (None
+    elsewhere).  headline: also the end-to-end leg and the CPU baseline."""
+    w, layers = make_workload(name, args.seed, args.num_seqs if headline else 0)
+    if args.layers > 0 and headline:
         layers = args.layers
     q8 = args.kv in ("q8_0", "fp8_e4m3")  # a quantised pool (q8_0 or E4M3)
     fp8 = args.kv == "fp8_e4m3"
@@ -305,9 +356,6 @@ def main():
     attn_b, app_b = bytes_per_layer(w, args.kv)
     step_bytes = layers * (attn_b + app_b)
     tokens_layers = int(w.context_lens.sum()) * w.q_len * layers if w.q_len > 1 else int(w.context_lens.sum()) * layers
-
-    if args.impl == "reference":
-        return run_reference(args, world, rank, w, layers, step_bytes)
 
     import paged_kv_decode_attention_gb300 as pkv
 
@@ -497,6 +545,7 @@ def main():
     # dependent launch; each call still waits for the previous one before it
     # reads its inputs), timed with one event pair over K replays ----
     attn_us = attn_us_isolated
+    clk_kernel = None
     sustained = graph is not None
     if sustained:
         def attention_layers():
@@ -511,18 +560,31 @@ def main():
             attn_graph.replay()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        # as many replays as fill about args.kernel_pass_s of GPU time (K at
+        # least), so that the clock samples taken meanwhile carry weight
         a0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(3):
             attn_graph.replay()
         a1.record(stream)
         torch.cuda.synchronize()
-        attn_us = a0.elapsed_time(a1) * 1e3 / (args.steps * layers)
+        reps = max(args.steps, int(math.ceil(args.kernel_pass_s * 1e3 / max(a0.elapsed_time(a1) / 3, 1e-3))))
+        kclocks = ClockSampler(local)
+        kclocks.start()
+        a0.record(stream)
+        for _ in range(reps):
+            attn_graph.replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        clk_kernel = kclocks.stop()
+        if clk_kernel is not None:
+            clk_kernel["replays"] = reps
+        attn_us = a0.elapsed_time(a1) * 1e3 / (reps * layers)
         if pkv.get_device_error(reset=True) != 0:
             raise RuntimeError("device error word set during the sustained kernel-timing pass")
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
-    if not args.no_e2e:
+    if headline and not args.no_e2e:
         p_q, p_kn, p_vn = h_q.pin_memory(), h_kn.pin_memory(), h_vn.pin_memory()
         p_tables, p_ctx, p_slots = h_tables.pin_memory(), h_ctx.pin_memory(), h_slots.pin_memory()
         p_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -610,19 +672,29 @@ def main():
 
     # ---- CPU oracle baseline (rank 0 at N=1 only) ----
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if headline and rank == 0 and world == 1 and not args.no_cpu_baseline:
         if q8:
             sub, kq_h, vq_h = oracle_sample_q8(w, k_pool[0], v_pool[0], max_seqs=w.num_seqs)
             r = time_oracle_q8(sub, kq_h, vq_h, budget_s=args.oracle_budget_s, kv=args.kv)
+            sub1, kq1, vq1 = oracle_sample_q8(w, k_pool[0], v_pool[0], max_seqs=2)
+            r1 = time_oracle_q8(sub1, kq1, vq1, budget_s=args.oracle_budget_s / 2, kv=args.kv, num_threads=1)
         else:
             sub = oracle_sample(w, k_pool[0], v_pool[0], max_seqs=w.num_seqs)
             r = time_oracle(sub, budget_s=args.oracle_budget_s)
+            sub1 = oracle_sample(w, k_pool[0], v_pool[0], max_seqs=2)
+            r1 = time_oracle(sub1, budget_s=args.oracle_budget_s / 2, num_threads=1)
         cpu = {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
                "sample": f"layer 0 of this workload ({r['seqs']} requests, append + attention), FP64 C oracle, "
-                         f"{r['reps']} repetitions, {r['s_per_layer_call'] * 1e3:.1f} ms per layer-call"}
+                         f"{r['reps']} repetitions, {r['s_per_layer_call'] * 1e3:.1f} ms per layer-call",
+               "single_core": {"value": round(r1["gbs"], 4), "unit": "GB/s", "cores": 1,
+                               "sample": f"layer 0, requests 0-{r1['seqs'] - 1} of this workload (append + "
+                                         f"attention), FP64 C oracle on one thread, {r1['reps']} repetitions, "
+                                         f"{r1['s_per_layer_call'] * 1e3:.1f} ms per sample"}}
 
+    if graph is not None:
+        graph.close()
     if rank != 0:
-        return
+        return None
     peaks = {}
     pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pp):
@@ -636,7 +708,7 @@ def main():
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
-        tj = json.load(open(tpath)).get(args.workload + ("_" + args.kv if q8 else ""))
+        tj = json.load(open(tpath)).get(name + ("_" + args.kv if q8 else ""))
         if tj and tj.get("kernel_build") == kernel_build_id():
             traffic = tj.get("bytes_per_launch")
     line = {
@@ -647,17 +719,11 @@ def main():
                   "f32 accumulation and softmax" if fp8 else
                   f"{args.kv} KV, f16 tensor-core Q.K, f32 softmax and P.V" if q8 else "bf16"),
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_seqs": b, "q_len": ql,
-                   "layers": layers, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16,
-                   "ctx_min": int(w.context_lens.min()), "ctx_max": int(w.context_lens.max()),
-                   "kv_format": args.kv,
-                   "kv_blocks_per_split": bps, "splits": splits, "cuda_graph": bool(graph is not None),
+        "config": workload_config(name, w, layers, args.kv, world),
+        "launch": {"kv_blocks_per_split": bps, "splits": splits, "cuda_graph": bool(graph is not None),
                    "cascade": ({"groups": int(gs_h.shape[0]), "prefix_blocks": maxp, "max_suffix_blocks": maxs,
                                 "prefix_blocks_per_split": pbps,
-                                "suffix_blocks_per_split": sbps} if cascade else None),
-                   "l2": "inputs larger than L2: one KV pool per layer, %.1f GB total" % (
-                       2 * k_pool.numel() * k_pool.element_size() / 1e9),
-                   "parallelism": f"replicas x{world}"},
+                                "suffix_blocks_per_split": sbps} if cascade else None)},
         "us_per_layer_call": round(attn_us, 3),
         "us_per_layer_call_isolated": round(attn_us_isolated, 3),
         "attention_tokens_layers_per_s": round(world * tokens_layers / (ms_per_step * 1e-3), 1),
@@ -681,8 +747,17 @@ def main():
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches_per_layer * layers * args.steps),
         "clocks": clk,
+        "clocks_kernel_pass": clk_kernel,
     }
-    print(json.dumps(line), flush=True)
+    return line
+
+
+def workload_config(name: str, w, layers: int, kv: str, world: int) -> dict:
+    """The JSON line's `config`: the workload alone (both arms report the same)."""
+    return {"workload": WORKLOAD_TEXT[name], "name": name, "num_seqs": w.num_seqs, "q_len": w.q_len,
+            "layers": layers, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": 16, "ctx_min": int(w.context_lens.min()), "ctx_max": int(w.context_lens.max()),
+            "kv_format": kv, "l2": l2_text(w, layers, kv), "parallelism": f"replicas x{world}"}
 
 
 def quantised_pools(pkv, kv: str, nb: int, seed: int, dev, chunk: int = 4096):
@@ -845,11 +920,7 @@ def run_reference(args, world, rank, w, layers, step_bytes):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "num_seqs": w.num_seqs,
-                       "q_len": w.q_len, "layers": layers, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
-                       "head_dim": w.head_dim, "block_size": 16, "ctx_min": int(w.context_lens.min()),
-                       "ctx_max": int(w.context_lens.max()), "kv_format": args.kv,
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(args.workload, w, layers, args.kv, world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
                              "cores": oracle.max_threads(), "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
