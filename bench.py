@@ -497,8 +497,8 @@ def bench_one(args, name: str, world: int, rank: int, local: int, headline: bool
             cascade={"num_groups": int(gs_h.shape[0]), "max_prefix_blocks": maxp, "max_suffix_blocks": maxs,
                      "prefix_blocks_per_split": pbps, "suffix_blocks_per_split": sbps} if cascade else None)
         run_step = lambda events=None: graph.launch(0, stream)
-        if ql == 1 and t_tok == b and (fp8 or (not q8 and (cascade or not tc_decode))):
-            launches_per_layer -= 1  # the graph's BF16 and E4M3 decode layers fuse the append into the attention
+        if ql == 1 and t_tok == b and (q8 or cascade or not tc_decode):
+            launches_per_layer -= 1  # the graph's decode layers fuse the append into the attention
     else:
         run_step = step
 

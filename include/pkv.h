@@ -455,6 +455,28 @@ pkv_status pkv_paged_attention_q8_0(void* out, const void* q, const void* k_cach
                                     int32_t num_q_heads, float scale, int32_t kv_blocks_per_split, void* workspace,
                                     size_t workspace_bytes, void* stream);
 
+/*
+ * pkv_paged_attention_q8_0_append -- pkv_kv_append_q8_0 followed by
+ * pkv_paged_attention_q8_0, in one call (arguments as for the two).  Ch8
+ * §8.1.1: a decode step stores the new token's K and V and reads the context
+ * KV, the new token included; §8.4.2 / Fig. 8-23: the stored form is q8_0.
+ * When num_tokens == num_seqs (token r is request r's new token, at position
+ * context_lens[r] - 1) the decode kernel quantises and stores the tokens
+ * itself, exactly as pkv_kv_append_q8_0 does, and uses them in place of the
+ * rows it read; other counts issue the append, then the attention.  A slot
+ * other than the one the block table gives that position is stored as the
+ * append would but sets PKV_DEVERR_SLOT (the result is then undefined); rows
+ * with context_lens[r] <= 0 (PKV_DEVERR_SLOT for a slot >= 0) or longer than
+ * the table store nothing.  Results equal the two calls' bit for bit
+ * otherwise.  Every host check runs before anything is enqueued.
+ */
+pkv_status pkv_paged_attention_q8_0_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                           const pkv_cache_desc* cache, const int32_t* block_tables,
+                                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                           int32_t num_q_heads, float scale, int32_t kv_blocks_per_split,
+                                           void* workspace, size_t workspace_bytes, const int64_t* slot_mapping,
+                                           const void* k_new, const void* v_new, int32_t num_tokens, void* stream);
+
 /* pkv_copy_blocks for q8_0 pools (num_kv_heads * PKV_Q8_TILE_BYTES per block). */
 pkv_status pkv_copy_blocks_q8_0(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
                                 const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,

@@ -26,7 +26,8 @@ __all__ = [
     "choose_kv_blocks_per_split", "get_device_error", "library_path", "lib", "DEVERR_BLOCK_ID",
     "DEVERR_SLOT", "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "Q8_TILE_BYTES", "kv_append_q8_0", "paged_attention_q8_0",
     "choose_kv_blocks_per_split_q8_0", "choose_kv_blocks_per_split_fp8_e4m3", "workspace_size_q8_0", "copy_blocks_q8_0", "FP8_TILE_BYTES",
-    "kv_append_fp8_e4m3", "paged_attention_fp8_e4m3", "paged_attention_fp8_e4m3_append", "copy_blocks_fp8_e4m3",
+    "kv_append_fp8_e4m3", "paged_attention_fp8_e4m3", "paged_attention_fp8_e4m3_append",
+    "paged_attention_q8_0_append", "copy_blocks_fp8_e4m3",
     "DecodeGraph", "KV_BF16", "KV_Q8_0", "KV_FP8_E4M3", "selftest_bounded_wait",
 ]
 
@@ -141,6 +142,8 @@ def _load():
     lib.pkv_paged_attention_fp8_e4m3_append.argtypes = [p, p, p, p, ctypes.POINTER(CacheDesc), p, i32, p, i32, i32,
                                                         f32, i32, p, sz, p, p, p, i32, p]
     lib.pkv_paged_attention_fp8_e4m3_append.restype = ctypes.c_int
+    lib.pkv_paged_attention_q8_0_append.argtypes = lib.pkv_paged_attention_fp8_e4m3_append.argtypes
+    lib.pkv_paged_attention_q8_0_append.restype = ctypes.c_int
     lib.pkv_decode_graph_create.argtypes = [ctypes.POINTER(DecodeGraphDesc), ctypes.POINTER(ctypes.c_void_p)]
     lib.pkv_decode_graph_create.restype = ctypes.c_int
     lib.pkv_decode_graph_launch.argtypes = [p, i32, p]
@@ -532,6 +535,34 @@ def paged_attention_q8_0(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tens
                                          ctypes.byref(desc), block_tables.data_ptr(), maxb, context_lens.data_ptr(),
                                          b, q.shape[2], float(scale), bps, ws_ptr, ws_bytes, _stream_ptr(stream)),
            "pkv_paged_attention_q8_0")
+
+
+def paged_attention_q8_0_append(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                slot_mapping: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                kv_blocks_per_split: int = 0, workspace: torch.Tensor | None = None,
+                                stream=None) -> None:
+    """kv_append_q8_0, then paged_attention_q8_0, as one call (one launch when each request appends its one new
+    token)."""
+    desc = _q8_pool(k_cache, "k_cache")
+    _q8_pool(v_cache, "v_cache")
+    _bf16(out, "out"), _bf16(q, "q"), _bf16(k_new, "k_new"), _bf16(v_new, "v_new")
+    _i32(block_tables, "block_tables"), _i32(context_lens, "context_lens")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous CUDA int64 tensor")
+    b = context_lens.numel()
+    if q.dim() != 4 or q.shape[0] != b or q.shape[1] != 1 or out.shape != q.shape:
+        raise ValueError("q/out must be [num_seqs][1][num_q_heads][head_dim]")
+    t = slot_mapping.numel()
+    if tuple(k_new.shape) != (t, desc.num_kv_heads, HEAD_DIM) or tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError("k_new/v_new must be [num_tokens][num_kv_heads][head_dim]")
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) if workspace is not None \
+        else (0, 0)
+    _check(_lib.pkv_paged_attention_q8_0_append(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), b, q.shape[2], float(scale),
+        int(kv_blocks_per_split), ws_ptr, ws_bytes, slot_mapping.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), t,
+        _stream_ptr(stream)), "pkv_paged_attention_q8_0_append")
 
 
 def copy_blocks_q8_0(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: torch.Tensor,

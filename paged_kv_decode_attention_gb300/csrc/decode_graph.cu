@@ -78,15 +78,20 @@ pkv_status attend_layer(const pkv_decode_graph_desc& d, const pkv_decode_graph_b
   }
 }
 
-// BF16 and E4M3 layers: the append and the attention as one call
-// (pkv_paged_attention_append, its cascade form, or the E4M3 one), which fuses
-// them into one kernel when it can.
+// The append and the attention as one call (pkv_paged_attention_append, its
+// cascade form, or the q8_0 / E4M3 one), which fuses them into one kernel
+// when it can.
 pkv_status append_attend_layer(const pkv_decode_graph_desc& d, const pkv_decode_graph_buffers& b, int l,
                                cudaStream_t s) {
   const size_t q_layer = static_cast<size_t>(d.num_seqs) * d.q_len * d.num_q_heads * kBf16RowBytes;
   const size_t kv_layer = static_cast<size_t>(d.num_tokens) * d.cache.num_kv_heads * kBf16RowBytes;
   const void* kn = static_cast<const uint8_t*>(b.k_new) + l * kv_layer;
   const void* vn = static_cast<const uint8_t*>(b.v_new) + l * kv_layer;
+  if (d.kv_format == PKV_KV_Q8_0)
+    return pkv_paged_attention_q8_0_append(
+        static_cast<uint8_t*>(b.out) + l * q_layer, static_cast<const uint8_t*>(b.q) + l * q_layer, d.k_caches[l],
+        d.v_caches[l], &d.cache, b.block_tables, d.max_blocks_per_seq, b.context_lens, d.num_seqs, d.num_q_heads,
+        d.scale, d.kv_blocks_per_split, d.workspace, d.workspace_bytes, b.slot_mapping, kn, vn, d.num_tokens, s);
   if (d.kv_format == PKV_KV_FP8_E4M3)
     return pkv_paged_attention_fp8_e4m3_append(
         static_cast<uint8_t*>(b.out) + l * q_layer, static_cast<const uint8_t*>(b.q) + l * q_layer, d.k_caches[l],
@@ -155,7 +160,7 @@ pkv_status pkv_decode_graph_create(const pkv_decode_graph_desc* desc, pkv_decode
     }
     pkv_status call = PKV_OK;
     for (int l = 0; l < d.num_layers && call == PKV_OK; ++l) {
-      if (d.num_tokens > 0 && d.kv_format != PKV_KV_Q8_0) {
+      if (d.num_tokens > 0) {
         call = append_attend_layer(d, d.set[s], l, cs);  // the append fused where the shape allows
         continue;
       }

@@ -84,18 +84,8 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(uint8_t* __restrict__
       continue;
     }
     const uint2 w = (which ? v_new : k_new)[(t * num_kv_heads + h) * (kHeadDim / 4) + lane];
-    const float x0 = bf16_lo(w.x), x1 = bf16_hi(w.x), x2 = bf16_lo(w.y), x3 = bf16_hi(w.y);
-    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-#pragma unroll
-    for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-    const int c0 = static_cast<int>(roundf(__fmul_rn(x0, id)));
-    const int c1 = static_cast<int>(roundf(__fmul_rn(x1, id)));
-    const int c2 = static_cast<int>(roundf(__fmul_rn(x2, id)));
-    const int c3 = static_cast<int>(roundf(__fmul_rn(x3, id)));
-    const uint32_t codes = (static_cast<uint32_t>(c0) & 0xffu) | ((static_cast<uint32_t>(c1) & 0xffu) << 8) |
-                           ((static_cast<uint32_t>(c2) & 0xffu) << 16) | (static_cast<uint32_t>(c3) << 24);
+    float d;
+    const uint32_t codes = q8_0_quantize_lane(w, d);
     const int64_t blk = slot / kBlockSize;
     const int off = static_cast<int>(slot % kBlockSize);
     uint8_t* tile = (which ? v_cache : k_cache) + (blk * num_kv_heads + h) * kQ8TileBytes;

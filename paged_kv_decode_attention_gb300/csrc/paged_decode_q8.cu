@@ -42,6 +42,11 @@
 //              FP16 operand tile (128-byte swizzled rows), the unit's Qbd, and
 //              a copy of the tile's K scales for the softmax, so that a K stage
 //              is free as soon as its codes are converted.
+// The fused-append instance (kFused) adds one warp: per unit holding its
+// request's new token it quantises the new K and V rows as kv_append_q8 does
+// and stores them in the pools, and the producers issue the copy of that
+// token's tile only after the rows are in place, so the tile carries them and
+// no other role changes.
 // Every wait is bounded (about 2 s) and reports PKV_DEVERR_TIMEOUT instead of
 // hanging; the roles exchange data only through mbarriers.
 #include <cmath>
@@ -72,6 +77,9 @@ constexpr int kFirstAttnWarp = kMmaWarp + 1;
 constexpr int kAttnWarps = 8;
 constexpr int kFirstDqWarp = kFirstAttnWarp + kAttnWarps;
 constexpr int kQ8Threads = (kFirstDqWarp + 4) * 32;
+constexpr int kAppendWarp = kFirstDqWarp + 4;        // fused-append instance only
+constexpr int kQ8ThreadsFused = kQ8Threads + 32;
+constexpr int kReadySlots = 4;                       // fused append: units whose new rows are stored, a ring
 constexpr int kQ8TileBlocks = 8;                               // blocks per 128-token tile
 constexpr int kRawStageBytes = kQ8TileBlocks * kQ8TileBytes;   // 8 K (or V) tiles: 17408
 constexpr int kOpHalfBytes = 128 * 128;                        // 128 rows x 64 FP16 values
@@ -98,15 +106,20 @@ struct Q8Bars {
   uint64_t s_full[2], s_empty[2];
   uint64_t sk_full[kScaleSlots];
   uint64_t merge[2];
+  uint64_t ready[kReadySlots], ready_empty[kReadySlots];  // fused append: a unit's new rows are in the pools
   uint32_t tmem_base;
 };
 static_assert(sizeof(Q8Bars) <= 512, "barrier area");
 
-// One (request, KV head, split) of the launch.
+// One (request, KV head, split) of the launch; with the append fused in,
+// also where the request's new token (position ctx - 1) falls: its tile of
+// the unit and its logical block (new_tile -1 when another unit holds it).
 struct Unit {
   int r, kvh, split, b0, b1, n_tiles, ctx_keys, ctx_raw;
+  int new_tile, new_blk;
 };
 
+template <bool kFused = false>
 __device__ __forceinline__ Unit unit_at(const DecodeArgs& a, int u) {
   Unit x;
   x.split = u % a.num_splits;
@@ -120,7 +133,29 @@ __device__ __forceinline__ Unit unit_at(const DecodeArgs& a, int u) {
   x.b1 = min(nb, x.b0 + a.blocks_per_split);
   x.n_tiles = x.b1 > x.b0 ? (x.b1 - x.b0 + kQ8TileBlocks - 1) / kQ8TileBlocks : 0;
   x.ctx_keys = min(ctx, x.b1 * kBlockSize);
+  x.new_tile = -1;
+  x.new_blk = 0;
+  if (kFused && x.ctx_raw > 0 && x.ctx_raw <= a.max_blocks * kBlockSize) {
+    const int nbl = (x.ctx_raw - 1) / kBlockSize;
+    if (nbl >= x.b0 && nbl < x.b1) {
+      x.new_tile = (nbl - x.b0) / kQ8TileBlocks;
+      x.new_blk = nbl;
+    }
+  }
   return x;
+}
+
+// Fused append: one warp stores its quantised row (lane l: codes of values
+// 4l .. 4l+3; lanes 8g: group g's scale) at `slot` of one pool, as
+// kv_append_q8 does; a slot outside the pool (or negative) stores nothing.
+__device__ __forceinline__ void q8_store_row(const DecodeArgs& a, const void* cache, int64_t slot, int kvh,
+                                             uint32_t codes, float d, int lane) {
+  if (slot < 0 || slot >= static_cast<int64_t>(a.num_blocks) * kBlockSize) return;
+  uint8_t* tile = static_cast<uint8_t*>(const_cast<void*>(cache)) +
+                  ((slot / kBlockSize) * a.num_kv_heads + kvh) * static_cast<int64_t>(kQ8TileBytes);
+  const int off = static_cast<int>(slot % kBlockSize);
+  *reinterpret_cast<uint32_t*>(tile + off * kHeadDim + lane * 4) = codes;
+  if ((lane & 7) == 0) *reinterpret_cast<__half*>(tile + kQ8CodeBytes + (off * 4 + (lane >> 3)) * 2) = __float2half_rn(d);
 }
 
 // Power-of-two shift e that brings the group's largest |q| below 2^15, so
@@ -197,7 +232,13 @@ __device__ __forceinline__ bool merge_sync(uint64_t* merge, uint32_t& n, int lan
 }
 
 // q8_0 tiles: int8 codes + FP16 group scales, 2176 B per (block, KV head).
-__global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const DecodeArgs a) {
+// kFused: the step's append fused in (a.k_new, a.v_new, a.slot_mapping set;
+// token r is request r's new token), with one more warp; an instance of its
+// own, so the plain decode carries none of it.
+template <bool kFused>
+__global__ void __launch_bounds__(kFused ? kQ8ThreadsFused : kQ8Threads, 1)
+    paged_decode_q8_kernel(const DecodeArgs a) {
+  static_assert(!kFused || kPerRing == 1, "the fused append's ready ring assumes one producer warp per ring");
   constexpr int kTile = kQ8TileBytes;
   pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -226,6 +267,10 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
       mbar_init(&bars->merge[s], kAttnWarps);
     }
     for (int s = 0; s < kScaleSlots; ++s) mbar_init(&bars->sk_full[s], 128);
+    for (int s = 0; s < kReadySlots; ++s) {
+      mbar_init(&bars->ready[s], 32);                      // the append warp
+      mbar_init(&bars->ready_empty[s], kProducerWarps);   // each producer warp, once it has waited
+    }
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -258,8 +303,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
     const uint8_t* pool = static_cast<const uint8_t*>(is_v ? a.v_cache : a.k_cache);
     const uint64_t policy = l2_policy_evict_first();
     int i = 0;
+    int nf = 0;  // units holding their request's new token so far (fused append)
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const Unit x = unit_at(a, u);
+      const Unit x = unit_at<kFused>(a, u);
       const int32_t* table = a.block_tables + static_cast<int64_t>(x.r) * a.max_blocks;
       // the load stays inside the table row whatever the context length, so it
       // need not wait for that length; entries past the unit's blocks are dropped
@@ -285,8 +331,15 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
         if (lane == 0) {
           if (is_v) ok = mbar_wait(&bars->k_full[i % kKStages], (i / kKStages) & 1);  // K(i) landed
           if (ok && i >= ns) ok = mbar_wait(&empty[st], ((i / ns) & 1) ^ 1);
+          if (kFused && ok && j == x.new_tile) {
+            // fused append: the tile holding the new token is copied only once
+            // the append warp has stored the new rows in the pools
+            ok = mbar_wait(&bars->ready[nf % kReadySlots], (nf / kReadySlots) & 1);
+            mbar_arrive(&bars->ready_empty[nf % kReadySlots]);
+          }
           if (ok) mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(nblk) * kTile);
         }
+        if (kFused && j == x.new_tile) ++nf;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (copies)
@@ -355,6 +408,11 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
       const int64_t orow0 = static_cast<int64_t>(x.r) * hq + x.kvh * kGroup;
       if (threadIdx.x == kFirstAttnWarp * 32 && x.split == 0 && x.kvh == 0 && x.ctx_raw > a.max_blocks * kBlockSize)
         report(a.err, PKV_DEVERR_CONTEXT);
+      // fused append: a slot for an empty row has no position ctx - 1 to go
+      // to; the token is not stored and the caller's error is reported
+      if (kFused && threadIdx.x == kFirstAttnWarp * 32 && x.split == 0 && x.kvh == 0 && x.ctx_raw <= 0 &&
+          a.slot_mapping[x.r] >= 0)
+        report(a.err, PKV_DEVERR_SLOT);
       const int64_t orow_out = orow0 + h_out;
       if (x.n_tiles == 0) {
         if (a.num_splits == 1)
@@ -521,8 +579,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
       ok = merge_sync(bars->merge, nmerge, lane);
     }
     if (!ok && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
-  } else {
-    // ------------------------------ K dequantisation (last 4 warps) ------------------------------
+  } else if (warp < kAppendWarp) {
+    // ------------------------------ K dequantisation (4 warps) ------------------------------
     const int t128 = threadIdx.x - kFirstDqWarp * 32;
     const int cc = t128 & 15;  // 16-byte output chunk of a row: dims 8cc .. 8cc+7
     const int rsub = t128 >> 4;
@@ -580,6 +638,39 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
       }
     }
     if (!ok && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
+  } else if constexpr (kFused) {
+    // ------------------------------ append (fused instance) ------------------------------
+    // Per unit holding its request's new token: the K and V rows quantised as
+    // kv_append_q8 quantises them and stored where it stores them, then made
+    // visible to the producers' bulk copies (async proxy) and announced; the
+    // tile holding the token is copied after that, so it carries the rows.
+    // A slot other than the one the block table gives position ctx - 1 is
+    // stored and reported (the result is then undefined, as documented).
+    int nf = 0;
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const Unit x = unit_at<true>(a, u);
+      if (x.new_tile < 0) continue;
+      const int sl = nf % kReadySlots;
+      if (nf >= kReadySlots)  // both producers have passed the slot's previous unit
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->ready_empty[sl], ((nf / kReadySlots) - 1) & 1));
+      if (!ok) break;
+      const int64_t row = static_cast<int64_t>(x.r) * a.num_kv_heads + x.kvh;
+      const uint2 kr = reinterpret_cast<const uint2*>(a.k_new)[row * (kHeadDim / 4) + lane];
+      const uint2 vr = reinterpret_cast<const uint2*>(a.v_new)[row * (kHeadDim / 4) + lane];
+      const int64_t slot = a.slot_mapping[x.r];
+      const int pb = a.block_tables[static_cast<int64_t>(x.r) * a.max_blocks + x.new_blk];
+      float kd, vd;
+      const uint32_t kc = q8_0_quantize_lane(kr, kd);
+      const uint32_t vc = q8_0_quantize_lane(vr, vd);
+      q8_store_row(a, a.k_cache, slot, x.kvh, kc, kd, lane);
+      q8_store_row(a, a.v_cache, slot, x.kvh, vc, vd, lane);
+      if (slot >= 0 && slot != static_cast<int64_t>(pb) * kBlockSize + (x.ctx_raw - 1) % kBlockSize && lane == 0)
+        report(a.err, PKV_DEVERR_SLOT);
+      fence_proxy_async_global();  // the stores before the bulk copies that read them
+      mbar_arrive(&bars->ready[sl]);
+      ++nf;
+    }
+    if (!ok && lane == 0) report(a.err, PKV_DEVERR_TIMEOUT);
   }
 
   tc::fence_before_sync();
@@ -590,6 +681,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) paged_decode_q8_kernel(const De
   }
 }
 
+template <bool kFused>
 cudaError_t allow_smem_q8() {
   static bool done[64];
   int dev = 0;
@@ -597,7 +689,7 @@ cudaError_t allow_smem_q8() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev]) {
-    e = cudaFuncSetAttribute(paged_decode_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ8);
+    e = cudaFuncSetAttribute(paged_decode_q8_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ8);
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
@@ -608,10 +700,16 @@ cudaError_t allow_smem_q8() {
 
 cudaError_t launch_paged_decode_q8(const DecodeArgs& a, int32_t grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  cudaError_t e = allow_smem_q8();
+  if (a.k_new != nullptr) {
+    cudaError_t e = allow_smem_q8<true>();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(paged_decode_q8_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kQ8ThreadsFused),
+                      kSmemQ8, stream, 1, a);
+  }
+  cudaError_t e = allow_smem_q8<false>();
   if (e != cudaSuccess) return e;
-  return launch_pdl(paged_decode_q8_kernel, dim3(static_cast<unsigned>(grid)), dim3(kQ8Threads), kSmemQ8, stream, 1,
-                    a);
+  return launch_pdl(paged_decode_q8_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kQ8Threads), kSmemQ8,
+                    stream, 1, a);
 }
 
 }  // namespace pkv

@@ -667,7 +667,7 @@ pkv_status quantised_attention(void* out, const void* q, const void* k_cache, co
   a.num_splits = splits;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.part_slots = splits;
-  if (fused != nullptr) {  // E4M3 only: the decode kernel stores the new tokens
+  if (fused != nullptr) {  // the decode kernel stores the new tokens
     a.slot_mapping = fused->slot_mapping;
     a.k_new = fused->k_new;
     a.v_new = fused->v_new;
@@ -723,13 +723,19 @@ pkv_status pkv_paged_attention_fp8_e4m3(void* out, const void* q, const void* k_
                              true);
 }
 
-pkv_status pkv_paged_attention_fp8_e4m3_append(void* out, const void* q, void* k_cache, void* v_cache,
-                                               const pkv_cache_desc* cache, const int32_t* block_tables,
-                                               int32_t max_blocks_per_seq, const int32_t* context_lens,
-                                               int32_t num_seqs, int32_t num_q_heads, float scale,
-                                               int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
-                                               const int64_t* slot_mapping, const void* k_new, const void* v_new,
-                                               int32_t num_tokens, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The quantising append and the decode over a quantised cache as one call:
+// one launch when token r is request r's new token, else the append, then
+// the attention.  Every check runs before anything is enqueued.
+pkv_status quantised_attention_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                      const pkv_cache_desc* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, float scale, int32_t kv_blocks_per_split, void* workspace,
+                                      size_t workspace_bytes, const int64_t* slot_mapping, const void* k_new,
+                                      const void* v_new, int32_t num_tokens, void* stream, bool fp8) {
   pkv_status st = check_cache(cache);
   if (st != PKV_OK) return st;
   if (num_tokens < 0) return PKV_ERR_SHAPE;
@@ -739,23 +745,50 @@ pkv_status pkv_paged_attention_fp8_e4m3_append(void* out, const void* q, void* k
          reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
       return PKV_ERR_UNSUPPORTED;
   }
-  // every check of the attention first, so an error enqueues nothing
   st = quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                           num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream, true, nullptr,
+                           num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream, fp8, nullptr,
                            true);
   if (st != PKV_OK) return st;
-  if (num_tokens == num_seqs && num_seqs > 0) {  // token r is request r's new token: one launch
+  if (num_tokens == num_seqs && num_seqs > 0) {
     const FusedAppend f{slot_mapping, k_new, v_new};
     return quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
                                num_seqs, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream,
-                               true, &f, false);
+                               fp8, &f, false);
   }
   if (num_tokens > 0) {
-    st = pkv_kv_append_fp8_e4m3(k_cache, v_cache, cache, slot_mapping, k_new, v_new, num_tokens, stream);
+    st = fp8 ? pkv_kv_append_fp8_e4m3(k_cache, v_cache, cache, slot_mapping, k_new, v_new, num_tokens, stream)
+             : pkv_kv_append_q8_0(k_cache, v_cache, cache, slot_mapping, k_new, v_new, num_tokens, stream);
     if (st != PKV_OK) return st;
   }
   return quantised_attention(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                             num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream, true);
+                             num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes, stream, fp8);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_q8_0_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                           const pkv_cache_desc* cache, const int32_t* block_tables,
+                                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                           int32_t num_q_heads, float scale, int32_t kv_blocks_per_split,
+                                           void* workspace, size_t workspace_bytes, const int64_t* slot_mapping,
+                                           const void* k_new, const void* v_new, int32_t num_tokens, void* stream) {
+  return quantised_attention_append(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                                    num_seqs, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes,
+                                    slot_mapping, k_new, v_new, num_tokens, stream, false);
+}
+
+pkv_status pkv_paged_attention_fp8_e4m3_append(void* out, const void* q, void* k_cache, void* v_cache,
+                                               const pkv_cache_desc* cache, const int32_t* block_tables,
+                                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                               int32_t num_seqs, int32_t num_q_heads, float scale,
+                                               int32_t kv_blocks_per_split, void* workspace, size_t workspace_bytes,
+                                               const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                                               int32_t num_tokens, void* stream) {
+  return quantised_attention_append(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                                    num_seqs, num_q_heads, scale, kv_blocks_per_split, workspace, workspace_bytes,
+                                    slot_mapping, k_new, v_new, num_tokens, stream, true);
 }
 
 pkv_status pkv_kv_append_fp8_e4m3(void* k_cache, void* v_cache, const pkv_cache_desc* cache,

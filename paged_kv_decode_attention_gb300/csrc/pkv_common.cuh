@@ -46,6 +46,12 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's generic-proxy global writes before later async-proxy
+// (bulk copy, TMA) reads of the same memory, issued after a synchronisation.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Make initialised barriers visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -150,6 +156,29 @@ __device__ __forceinline__ float exp2_approx(float x) {
 
 __device__ __forceinline__ void report(unsigned int* err, unsigned int bit) {
   if (err) atomicOr(err, bit);
+}
+
+// q8_0 quantisation of one 128-value row by one warp ("Chapter 8: Inference
+// Optimization" §8.4.2, Fig. 8-23: groups of 32 values share one FP16
+// scale, 8-bit codes).  Lane l holds values 4l .. 4l+3 (two BF16 pairs), so
+// lanes 8g .. 8g+7 hold group g.  Per group d = max|x| / 127 and code =
+// round-half-away-from-zero(x * (1/d)), every step one IEEE-rounded FP32
+// operation (a zero group gets d = 0 and codes 0).  Returns the lane's 4
+// codes (byte k = value 4l + k) and sets d, the group's scale before its
+// FP16 rounding (the stored scale is __float2half_rn(d)).
+__device__ __forceinline__ uint32_t q8_0_quantize_lane(uint2 w, float& d) {
+  const float x0 = bf16_lo(w.x), x1 = bf16_hi(w.x), x2 = bf16_lo(w.y), x3 = bf16_hi(w.y);
+  float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  d = __fdiv_rn(amax, 127.0f);
+  const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+  const int c0 = static_cast<int>(roundf(__fmul_rn(x0, id)));
+  const int c1 = static_cast<int>(roundf(__fmul_rn(x1, id)));
+  const int c2 = static_cast<int>(roundf(__fmul_rn(x2, id)));
+  const int c3 = static_cast<int>(roundf(__fmul_rn(x3, id)));
+  return (static_cast<uint32_t>(c0) & 0xffu) | ((static_cast<uint32_t>(c1) & 0xffu) << 8) |
+         ((static_cast<uint32_t>(c2) & 0xffu) << 16) | (static_cast<uint32_t>(c3) << 24);
 }
 
 }  // namespace pkv

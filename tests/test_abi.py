@@ -236,10 +236,11 @@ def test_paged_attention_append_argument_errors():
              None) == 3  # k_new not 16-byte aligned
 
 
-def test_paged_attention_fp8_e4m3_append_argument_errors():
-    """The E4M3 append-and-attention call checks its own arguments on the
-    host before anything else (no CUDA call on these paths)."""
-    f = pkv.lib().pkv_paged_attention_fp8_e4m3_append
+@pytest.mark.parametrize("name", ["pkv_paged_attention_fp8_e4m3_append", "pkv_paged_attention_q8_0_append"])
+def test_paged_attention_quantised_append_argument_errors(name):
+    """The E4M3 and q8_0 append-and-attention calls check their own arguments
+    on the host before anything else (no CUDA call on these paths)."""
+    f = getattr(pkv.lib(), name)
     d = _desc()
     # no cache descriptor; a negative token count; new tokens without their K; a misaligned K
     assert f(None, None, None, None, None, None, 1, None, 1, 32, 1.0, 0, None, 0, None, None, None, 0, None) == 1

@@ -479,3 +479,192 @@ def test_fused_empty_row_with_a_slot_stores_nothing_and_sets_the_error_word():
 
 def test_fused_fp8_empty_row_with_a_slot_stores_nothing_and_sets_the_error_word():
     _empty_row_with_slot(fp8=True)
+
+
+# ---------------------------------------------------------------------------
+# q8_0: the append fused into the q8_0 decode kernel (pkv_paged_attention_q8_0_append)
+# ---------------------------------------------------------------------------
+
+def _q8_host_pools(k_pool: np.ndarray, v_pool: np.ndarray):
+    """q8_0 pools holding BF16 host pools, stored by the oracle's quantising append."""
+    nb, hkv = k_pool.shape[:2]
+    kq = np.zeros((nb, hkv, oracle.Q8_TILE_BYTES), np.uint8)
+    vq = np.zeros_like(kq)
+    oracle.kv_append_q8_0(kq, vq, np.arange(nb * 16, dtype=np.int64), _tokens_of_pool(k_pool),
+                          _tokens_of_pool(v_pool))
+    return kq, vq
+
+
+def _q8_oracle(w, kq: np.ndarray, vq: np.ndarray):
+    """The step with the oracle on copies of host q8_0 pools: the quantising
+    append of the new tokens, then FP64 attention over the stored values."""
+    kq, vq = kq.copy(), vq.copy()
+    oracle.kv_append_q8_0(kq, vq, w.slot_mapping, w.k_new, w.v_new)
+    out = oracle.paged_attention_f64(w.q, oracle.dequantize_q8_0(kq), oracle.dequantize_q8_0(vq), w.block_tables,
+                                     w.context_lens, 1, w.scale)
+    return out, kq, vq
+
+
+def _q8_both(w, bps=0):
+    d = to_device(w)
+    kh, vh = _q8_host_pools(w.k_cache, w.v_cache)
+    kq, vq = torch.from_numpy(kh).cuda(), torch.from_numpy(vh).cuda()
+    maxb = w.max_blocks_per_seq
+    if bps == 0:
+        bps = pkv.choose_kv_blocks_per_split_q8_0(w.num_seqs, w.num_kv_heads, maxb)
+    ws = torch.empty(max(pkv.workspace_size_q8_0(w.num_seqs, w.num_q_heads, maxb, bps), 256), dtype=torch.uint8,
+                     device="cuda")
+    res = []
+    for fused in (True, False):
+        kc, vc = kq.clone(), vq.clone()
+        out = torch.full_like(d["q"], float("nan"))
+        if fused:
+            pkv.paged_attention_q8_0_append(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
+                                            d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=bps,
+                                            workspace=ws)
+        else:
+            pkv.kv_append_q8_0(kc, vc, d["slot_mapping"], d["k_new"], d["v_new"])
+            pkv.paged_attention_q8_0(out, d["q"], kc, vc, d["block_tables"], d["context_lens"], w.scale,
+                                     kv_blocks_per_split=bps, workspace=ws)
+        torch.cuda.synchronize()
+        res.append((out, kc, vc))
+    return res, (kh, vh)
+
+
+def _assert_q8(res, host, w, what):
+    (of, kf, vf), (os_, ks, vs) = res
+    assert torch.equal(of.view(torch.int16), os_.view(torch.int16)), f"{what}: outputs differ"
+    assert torch.equal(kf, ks) and torch.equal(vf, vs), f"{what}: q8_0 pools differ"
+    ref, kq, vq = _q8_oracle(w, *host)
+    assert np.array_equal(kf.cpu().numpy(), kq) and np.array_equal(vf.cpu().numpy(), vq), \
+        f"{what}: q8_0 pools differ from the oracle's append"
+    assert_close(bf16_to_f64(of), ref, what=f"{what} vs oracle")
+
+
+# new tokens at every row of a 128-token tile modulo 8 and in each of its four
+# 32-row quarters (the dequantisation warp and the attention warp that take
+# the row), at a block's first and last slot, alone, and a padding row
+RAGGED_Q8 = [17, 300, 1, 16, 700, 0, 32, 2049, 129, 200, 4000, 46, 87, 110, 128, 77, 94, 123, 42]
+
+
+@pytest.mark.parametrize("bps", [0, 8, 24, 5, 1000])
+def test_fused_q8_equals_append_then_attention_and_oracle(bps):
+    ctx = np.asarray(RAGGED_Q8)
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("fused-q8", ctx, need + 30, seed=73)
+    res, host = _q8_both(w, bps)
+    _assert_q8(res, host, w, f"fused q8_0 bps={bps}")
+    assert not res[0][0][ctx == 0].float().abs().sum()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fused_q8_random_shapes(seed):
+    rng = np.random.default_rng(7000 + seed)
+    b = int(rng.integers(1, 61))
+    ctx = rng.integers(0, 3001, size=b)
+    ctx[rng.random(b) < 0.1] = 0
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("fused-q8-rand", ctx, need + 16, seed=8000 + seed)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[rng.random(b) < 0.1] = -1
+    bps = int(rng.choice([0, 0, 8, 16, 40, 1000]))
+    res, host = _q8_both(w, bps)
+    _assert_q8(res, host, w, f"q8_0 random seed={seed} b={b} bps={bps}")
+
+
+def test_fused_q8_wrong_slot_sets_the_error_word():
+    ctx = np.asarray([100, 200, 300])
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("bad-slot-q8", ctx, need + 30, seed=74)
+    used = set()
+    for r, c in enumerate(ctx):
+        used.update(int(b) for b in w.block_tables[r, :-(-int(c) // 16)])
+    spare = next(b for b in range(w.num_blocks) if b not in used)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[2] = spare * 16 + 5
+    d = to_device(w)
+    kh, vh = _q8_host_pools(w.k_cache, w.v_cache)
+    kq, vq = torch.from_numpy(kh).cuda(), torch.from_numpy(vh).cuda()
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(d["q"])
+    pkv.paged_attention_q8_0_append(out, d["q"], kq, vq, d["block_tables"], d["context_lens"], w.scale,
+                                    d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=1000, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(reset=True) == pkv.DEVERR_SLOT
+    # stored where the slot says, as the append would
+    ref_k, ref_v = kh.copy(), vh.copy()
+    oracle.kv_append_q8_0(ref_k, ref_v, w.slot_mapping, w.k_new, w.v_new)
+    assert np.array_equal(kq.cpu().numpy()[spare], ref_k[spare]) and np.array_equal(vq.cpu().numpy()[spare],
+                                                                                     ref_v[spare])
+
+
+def test_fused_q8_empty_row_with_a_slot_stores_nothing_and_sets_the_error_word():
+    ctx = np.asarray([100, 0, 300])
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("empty-row-q8", ctx, need + 30, seed=75)
+    used = set()
+    for r, c in enumerate(ctx):
+        used.update(int(b) for b in w.block_tables[r, :-(-int(c) // 16)])
+    spare = next(b for b in range(w.num_blocks) if b not in used)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[1] = spare * 16 + 7
+    d = to_device(w)
+    kh, vh = _q8_host_pools(w.k_cache, w.v_cache)
+    kq, vq = torch.from_numpy(kh).cuda(), torch.from_numpy(vh).cuda()
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out = torch.full_like(d["q"], float("nan"))
+    pkv.paged_attention_q8_0_append(out, d["q"], kq, vq, d["block_tables"], d["context_lens"], w.scale,
+                                    d["slot_mapping"], d["k_new"], d["v_new"], kv_blocks_per_split=1000, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(reset=True) == pkv.DEVERR_SLOT
+    assert np.array_equal(kq.cpu().numpy()[spare], kh[spare]) and np.array_equal(vq.cpu().numpy()[spare], vh[spare])
+    assert not out[1].float().abs().sum()
+    w.slot_mapping[1] = -1
+    assert_close(bf16_to_f64(out), _q8_oracle(w, kh, vh)[0], what="rows beside an empty q8_0 row with a slot")
+
+
+def test_fused_q8_short_chat_full_size():
+    """The 2K-context batch at full size (37 requests, 5461-block pools filled
+    on the device and quantised by the append) in the benchmark's launch
+    configuration: the fused call equals the append followed by the attention,
+    outputs and pools bit for bit, and sampled requests match the oracle."""
+    w = W.short_chat(seed=25, fill_cache=False)
+    nb, hkv = w.num_blocks, w.num_kv_heads
+    kb = torch.empty((nb, hkv, 16, 128), dtype=torch.bfloat16, device="cuda")
+    vb = torch.empty_like(kb)
+    W.fill_pool_device(kb, seed=25)
+    W.fill_pool_device(vb, seed=26)
+    tok = lambda p: p.permute(0, 2, 1, 3).contiguous().view(nb * 16, hkv, 128)
+    kq = torch.empty((nb, hkv, pkv.Q8_TILE_BYTES), dtype=torch.uint8, device="cuda")
+    vq = torch.empty_like(kq)
+    pkv.kv_append_q8_0(kq, vq, torch.arange(nb * 16, dtype=torch.int64, device="cuda"), tok(kb), tok(vb))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q, kn, vn = (dev(x).view(torch.bfloat16) for x in (w.q, w.k_new, w.v_new))
+    tables, ctx, slots = dev(w.block_tables), dev(w.context_lens), dev(w.slot_mapping)
+    maxb = w.max_blocks_per_seq
+    bps = pkv.choose_kv_blocks_per_split_q8_0(w.num_seqs, hkv, maxb)
+    ws = torch.empty(max(pkv.workspace_size_q8_0(w.num_seqs, w.num_q_heads, maxb, bps), 256), dtype=torch.uint8,
+                     device="cuda")
+    kf, vf = kq.clone(), vq.clone()
+    out_s, out_f = torch.full_like(q, float("nan")), torch.full_like(q, float("nan"))
+    pkv.kv_append_q8_0(kq, vq, slots, kn, vn)
+    pkv.paged_attention_q8_0(out_s, q, kq, vq, tables, ctx, w.scale, kv_blocks_per_split=bps, workspace=ws)
+    pkv.paged_attention_q8_0_append(out_f, q, kf, vf, tables, ctx, w.scale, slots, kn, vn, kv_blocks_per_split=bps,
+                                    workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_f.view(torch.int16), out_s.view(torch.int16)), "full-size q8_0: outputs differ"
+    assert torch.equal(kf, kq) and torch.equal(vf, vq), "full-size q8_0: pools differ"
+    got = bf16_to_f64(out_f)
+    for r in [0, 17, 36]:
+        n = -(-int(w.context_lens[r]) // 16)
+        idx = torch.from_numpy(w.block_tables[r, :n].astype(np.int64)).cuda()
+        sub = lambda p: p.index_select(0, idx).cpu().view(torch.int16).numpy().view(np.uint16)
+        kq_ref, vq_ref = _q8_host_pools(sub(kb), sub(vb))
+        slot = int(w.slot_mapping[r])
+        sub_slot = np.array([(n - 1) * 16 + slot % 16], np.int64)
+        oracle.kv_append_q8_0(kq_ref, vq_ref, sub_slot, w.k_new[r:r + 1], w.v_new[r:r + 1])
+        assert np.array_equal(kf.index_select(0, idx).cpu().numpy(), kq_ref) and \
+            np.array_equal(vf.index_select(0, idx).cpu().numpy(), vq_ref), f"request {r}: q8_0 pool bytes"
+        ref = oracle.paged_attention_f64(w.q[r:r + 1], oracle.dequantize_q8_0(kq_ref), oracle.dequantize_q8_0(vq_ref),
+                                         np.arange(n, dtype=np.int32)[None, :], w.context_lens[r:r + 1], 1, w.scale)
+        assert_close(got[r:r + 1], ref, what=f"full-size fused q8_0 request {r} vs oracle")
