@@ -11,11 +11,13 @@
 // tile), so S = Q K^T and O = P V run as tcgen05.mma with FP32 accumulators in
 // tensor memory, and softmax runs in FP32 on the CUDA cores in between.
 //
-// CTA = 6 warps, one (request, row tile, split, KV head); 2 CTAs per SM:
-//   warp 0  : TMA producer.  A KV tile is 4 blocks (64 tokens): for each block
-//             two 16x64 boxes of K and two of V (128-byte swizzle), issued by
-//             16 lanes at once, land in the KV ring; blocks past the range are
-//             fetched at an out-of-range row so TMA fills them with zeros.
+// CTA = 7 warps, one (request, row tile, split, KV head); 2 CTAs per SM:
+//   warps 0, 6: TMA producers of K and of V.  A tile is 4 blocks (64 tokens):
+//             for each block two 16x64 boxes (128-byte swizzle), issued by 8
+//             lanes at once, land in that tensor's ring; blocks past the range
+//             are fetched at an out-of-range row so TMA fills them with zeros.
+//             A K stage is free once S has read it, a V stage once P.V has, so
+//             the K ring refills while a tile's softmax and P.V still run.
 //   warp 1  : MMA issuer (one thread).  S_j = Q K_j^T (M 64, N 64, 8 k-steps,
 //             Q and K from shared memory) into a double-buffered TMEM S;
 //             O += P_j V_j (M 64, N 128, 2 x 4 k-steps, P from TMEM, V from
@@ -44,20 +46,22 @@
 namespace pkv {
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
+constexpr int kVProdWarp = 6;
 constexpr int kTileBlocks = 4;                        // KV blocks per tile
 constexpr int kTileTokens = kTileBlocks * kBlockSize;  // 64
 constexpr int kRows = 64;                             // 16 positions x 4 heads
 constexpr int kQBytes = kRows * kHeadDim * 2;         // 16 KiB
 constexpr int kHalfBytes = kTileTokens * 128;         // 64 tokens x 64 dims = 8 KiB
-constexpr int kStageBytesTc = 4 * kHalfBytes;         // K lo/hi, V lo/hi: 32 KiB
+constexpr int kStageBytesTc = 2 * kHalfBytes;         // K (or V) of a tile, dims 0-63 then 64-127: 16 KiB
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-// KV ring depth (32 KiB per stage): with P kept in tensor memory, 16 KiB of
-// Q plus 3 stages fit twice into an SM's shared memory (2 CTAs per SM, 96 KiB
-// of K/V in flight each).
+// Ring depth (16 KiB per stage, a K ring and a V ring): with P kept in
+// tensor memory, 16 KiB of Q plus 3 + 3 stages fit twice into an SM's shared
+// memory (2 CTAs per SM, 96 KiB of K/V each).
 constexpr int kTcStages = 3;
-constexpr int kOffBar = kOffKV + kTcStages * kStageBytesTc;
+constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffV = kOffK + kTcStages * kStageBytesTc;
+constexpr int kOffBar = kOffV + kTcStages * kStageBytesTc;
 constexpr int kSmemTc = kOffBar + 256;
 static_assert(kSmemTc <= 113 * 1024, "two CTAs per SM");
 // Tensor memory: two S/P buffers of 64 columns (S_j in FP32; then P_j over
@@ -70,8 +74,10 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units: weights stay below 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct TcBars {
-  uint64_t kv_full[kTcStages];
-  uint64_t kv_empty[kTcStages];
+  uint64_t k_full[kTcStages];
+  uint64_t k_empty[kTcStages];
+  uint64_t v_full[kTcStages];
+  uint64_t v_empty[kTcStages];
   uint64_t s_full[kNB];
   uint64_t p_full[kNB];
   uint64_t o_done[kNB];
@@ -87,6 +93,39 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
   TcBars* bars = reinterpret_cast<TcBars*>(smem + kOffBar);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+
+  // ---------------- set-up: barriers, TMEM (reads no input) ----------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int s = 0; s < kNB; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->o_done[s], 1);
+    }
+    mbar_init(&bars->q_full, 128);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tensor_map(&k_map);
+    tc::prefetch_tensor_map(&v_map);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  // everything below may read what earlier grids in the stream write; the
+  // grids launched after this one may start only now: the cascade's suffix
+  // pass reads its inputs without waiting, so they must be complete when it starts
+  pdl_wait();
+  pdl_trigger();
 
   const bool cascade = a.group_seqs != nullptr;
   const int n_rt = (a.q_len + 15) / 16;  // row tiles per request (chunk mode)
@@ -130,12 +169,17 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
   const int quad = warp & 3;
   const int half = lane >> 4;
   const int row = quad * 16 + (lane & 15);
-  const int rq = warp >= 2 ? row_req(row) : -1;
+  const bool softmax_warp = warp >= 2 && warp < 6;
+  const int rq = softmax_warp ? row_req(row) : -1;
   const int ip = row_pos(row);
   const int g = row & 3;
-  const bool row_valid = warp >= 2 && rq >= 0 && ip < a.q_len;
+  const bool row_valid = softmax_warp && rq >= 0 && ip < a.q_len;
   const int64_t orow = (static_cast<int64_t>(rq) * a.q_len + ip) * hq + kvh * kGroup + g;
   const int64_t slot = orow * a.part_slots + a.part_slot0 + split;
+
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t sbase = smem_addr(smem);
+  bool ok = true;
 
   if (n_tiles <= 0) {
     if (row_valid && half == 0) {
@@ -147,40 +191,13 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
         for (int c = 0; c < kHeadDim * 2 / 16; ++c) o[c] = make_uint4(0, 0, 0, 0);
       }
     }
-    return;
-  }
-
-  // ---------------- set-up: barriers, TMEM ----------------
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
-    }
-    for (int s = 0; s < kNB; ++s) {
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 128);
-      mbar_init(&bars->o_done[s], 1);
-    }
-    mbar_init(&bars->q_full, 128);
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(&bars->tmem_base, kTmemCols);
-    tc::tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    tc::prefetch_tensor_map(&k_map);
-    tc::prefetch_tensor_map(&v_map);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = bars->tmem_base;
-  const uint32_t sbase = smem_addr(smem);
-  bool ok = true;
-
-  if (warp == 0) {
-    // ---------------------------- TMA producer ----------------------------
+  } else if (warp == 0 || warp == kVProdWarp) {
+    // ---------------------------- TMA producers ----------------------------
+    const bool is_v = warp == kVProdWarp;
+    uint64_t* full = is_v ? bars->v_full : bars->k_full;
+    uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+    uint8_t* ring = smem + (is_v ? kOffV : kOffK);
+    const CUtensorMap* map = is_v ? &v_map : &k_map;
     const uint64_t policy = l2_policy_evict_first();
     const int32_t* table = a.block_tables + static_cast<int64_t>(table_row) * a.max_blocks;
     const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;  // first row past the pool
@@ -199,31 +216,28 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
     };
     // Block ids are read 32 at a time (8 tiles), one chunk ahead, and checked
     // only when their chunk is used, so the next chunk's load stays in flight.
-    // The 16 boxes of a tile (4 blocks x K/V x two 64-dim halves) are issued
-    // by 16 lanes at once: lane 4b + c takes block b, piece c (K lo, K hi,
-    // V lo, V hi).
+    // The 8 boxes of a tile (4 blocks x two 64-dim halves) are issued by 8
+    // lanes at once: lane 2b + c takes block b, half c.
     int cur = row_of(chunk(0)), nxt = INT_MIN;
     for (int j = 0; j < n_tiles && ok; ++j) {
       const int slot = j & 7;
       if (slot == 0) nxt = chunk((j + 8) * kTileBlocks);
-      const int yy = __shfl_sync(0xffffffffu, cur, slot * kTileBlocks + ((lane >> 2) & 3));
+      const int yy = __shfl_sync(0xffffffffu, cur, slot * kTileBlocks + ((lane >> 1) & 3));
       if (slot == 7) cur = row_of(nxt);
       const int st = j % kTcStages;
-      if (j >= kTcStages) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_empty[st], ((j / kTcStages) & 1) ^ 1));
+      if (j >= kTcStages) ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((j / kTcStages) & 1) ^ 1));
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytesTc);
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], kStageBytesTc);
       __syncwarp();
-      if (lane < 4 * kTileBlocks) {
-        const int b = lane >> 2, c = lane & 3;
-        tc::tma_load_2d(smem + kOffKV + st * kStageBytesTc + c * kHalfBytes + b * 2048, c < 2 ? &k_map : &v_map,
-                        (c & 1) * 64, yy, &bars->kv_full[st], policy);
+      if (lane < 2 * kTileBlocks) {
+        const int b = lane >> 1, c = lane & 1;
+        tc::tma_load_2d(ring + st * kStageBytesTc + c * kHalfBytes + b * 2048, map, c * 64, yy, &full[st], policy);
       }
     }
     if (lane == 0) {
       if (!ok) report(a.err, PKV_DEVERR_TIMEOUT);
       // the last tiles' copies must land before shared memory is released
-      for (int j = max(0, n_tiles - kTcStages); j < n_tiles; ++j)
-        mbar_wait(&bars->kv_full[j % kTcStages], (j / kTcStages) & 1);
+      for (int j = max(0, n_tiles - kTcStages); j < n_tiles; ++j) mbar_wait(&full[j % kTcStages], (j / kTcStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------- MMA issuer ----------------------------
@@ -240,11 +254,11 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
         bool progressed = false;
         if (js < n_tiles) {
           const int st = js % kTcStages, sb = js % kNB;
-          bool ready = mbar_test_wait(&bars->kv_full[st], (js / kTcStages) & 1);
+          bool ready = mbar_test_wait(&bars->k_full[st], (js / kTcStages) & 1);
           if (ready && js >= kNB) ready = mbar_test_wait(&bars->o_done[sb], ((js / kNB) - 1) & 1);
           if (ready) {
             tc::fence_after_sync();
-            const uint32_t kst = sbase + kOffKV + st * kStageBytesTc;
+            const uint32_t kst = sbase + kOffK + st * kStageBytesTc;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t qa = sbase + kOffQ + (kk >> 2) * 8192 + 32 * (kk & 3);
@@ -252,16 +266,18 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
               tc::mma_bf16(tmem + sb * 64, tc::smem_desc(qa, 16, 1024), tc::smem_desc(ka, 16, 1024), kIdS, kk > 0);
             }
             tc::commit(&bars->s_full[sb]);
+            tc::commit(&bars->k_empty[st]);
             ++js;
             progressed = true;
           }
         }
-        if (jp < js && mbar_test_wait(&bars->p_full[jp % kNB], (jp / kNB) & 1)) {
+        if (jp < js && mbar_test_wait(&bars->p_full[jp % kNB], (jp / kNB) & 1) &&
+            mbar_test_wait(&bars->v_full[jp % kTcStages], (jp / kTcStages) & 1)) {
           tc::fence_after_sync();
           const int st = jp % kTcStages;
           // P_jp: 64 BF16 high parts per row packed in 32 columns, then the remainders
           const uint32_t ptm = tmem + (jp % kNB) * 64;
-          const uint32_t vst = sbase + kOffKV + st * kStageBytesTc + 2 * kHalfBytes;
+          const uint32_t vst = sbase + kOffV + st * kStageBytesTc;
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -270,7 +286,7 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
                                   tc::smem_desc(vst + 2048 * kk, kHalfBytes, 1024), kIdO,
                                   (jp > 0 || part > 0 || kk > 0) ? 1u : 0u);
           tc::commit(&bars->o_done[jp % kNB]);
-          tc::commit(&bars->kv_empty[st]);
+          tc::commit(&bars->v_empty[st]);
           ++jp;
           progressed = true;
         }
@@ -396,9 +412,12 @@ __device__ __forceinline__ void paged_chunk_tc_body(const CUtensorMap& k_map, co
       const int tile0 = (b0 + j * kTileBlocks) * kBlockSize;
       const int tile_end = tile0 + kTileTokens;
       if (ctx_keys < tile_end && ctx_keys > tile0 && (ctx_keys & (kBlockSize - 1)) != 0) {
+        // V(j) may land after S(j): wait for it (its stage cannot move on
+        // before this tile's P.V, which waits for these weights)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (j / kTcStages) & 1));
         const int first = ctx_keys - tile0;                                // first garbage token of the tile
         const int last = min(kTileTokens, ((first + kBlockSize - 1) / kBlockSize) * kBlockSize);
-        uint8_t* vt = smem + kOffKV + st * kStageBytesTc + 2 * kHalfBytes;
+        uint8_t* vt = smem + kOffV + st * kStageBytesTc;
         const int t128 = threadIdx.x - 64;
         for (int idx = t128; idx < (last - first) * 16; idx += 128) {
           const int tk = first + (idx >> 4);
@@ -461,9 +480,7 @@ template <bool kSplit>
 __global__ void __launch_bounds__(kTcThreads, 2)
     paged_chunk_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                           const ChunkArgs a) {
-  pdl_wait();  // inputs come from earlier grids in the stream
-  pdl_trigger();
-  paged_chunk_tc_body<kSplit>(k_map, v_map, a);
+  paged_chunk_tc_body<kSplit>(k_map, v_map, a);  // waits for earlier grids after its set-up
 }
 
 // ---------------------------------------------------------------------------

@@ -84,9 +84,10 @@ struct DecodeArgs {
   const float* prefix_o;
   const float* prefix_lse;
   int32_t prefix_slots;
-  // Decode launched right after the cascade's prefix pass: its inputs were
-  // complete before that pass started, so it starts at once (overlapping the
-  // pass) and waits for the pass only before it exits.
+  // Decode launched right after the cascade's prefix pass: that pass lets
+  // the grids after it start only once it has waited for the grids before it,
+  // so this decode's inputs are complete when it starts; it starts at once
+  // (overlapping the pass) and waits for the pass only before it exits.
   int32_t overlap_previous;
   // Append fused into the decode kernel (q_len 1, CTA-per-row kernel): token
   // r of k_new/v_new ([num_seqs][Hkv][128] BF16) is request r's new token, at
