@@ -315,6 +315,16 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
           if (!ok) break;
         }
       }
+      // Cascade: with every copy issued, this warp waits for the prefix pass
+      // and pulls the row's prefix partials into L1, so that the merge at the
+      // end (in the CTA that merges) finds them there instead of in L2.
+      if (has_prefix && (kMode == SplitMode::kDirect || (kMode == SplitMode::kCluster && cluster_cta_rank() == 0))) {
+        pdl_wait();
+        const char* po = reinterpret_cast<const char*>(a.prefix_o + qrow0 * a.prefix_slots * kHeadDim);
+        const int bytes = kGroup * a.prefix_slots * kHeadDim * static_cast<int>(sizeof(float));
+        for (int off = lane * 128; off < bytes; off += 32 * 128) prefetch_l1(po + off);
+        if (lane == 0) prefetch_l1(a.prefix_lse + qrow0 * a.prefix_slots);
+      }
       if (lane == 0) {
         if (!ok) report(a.err, PKV_DEVERR_TIMEOUT);
         // every issued copy must land before the CTA's shared memory is released
@@ -579,20 +589,35 @@ __device__ __forceinline__ void paged_decode_body(const DecodeArgs& a) {
       const int h = warp;
       const int d0 = lane * 4;
       const uint32_t nranks = gridDim.y;  // cluster = all splits of this (row, KV head)
+      // every rank's (max, sum, O) read at once: one round trip over the cluster
+      float mr[kMaxClusterSplits], lr[kMaxClusterSplits];
+      float4 vr[kMaxClusterSplits];
+#pragma unroll
+      for (int rk = 0; rk < kMaxClusterSplits; ++rk) {
+        if (rk < static_cast<int>(nranks)) {
+          mr[rk] = ld_cluster_f32(map_shared_to_rank(cta_m + h, rk));
+          lr[rk] = ld_cluster_f32(map_shared_to_rank(cta_l + h, rk));
+          vr[rk] = ld_cluster_f32x4(map_shared_to_rank(cta_o + h * kHeadDim + d0, rk));
+        } else {
+          mr[rk] = -INFINITY;
+          lr[rk] = 0.f;
+          vr[rk] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
       float mx = -INFINITY;
-      for (uint32_t rk = 0; rk < nranks; ++rk) mx = fmaxf(mx, ld_cluster_f32(map_shared_to_rank(cta_m + h, rk)));
+#pragma unroll
+      for (int rk = 0; rk < kMaxClusterSplits; ++rk) mx = fmaxf(mx, mr[rk]);
       float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f, sum = 0.f;
       if (mx != -INFINITY) {
-        for (uint32_t rk = 0; rk < nranks; ++rk) {
-          const float m = ld_cluster_f32(map_shared_to_rank(cta_m + h, rk));
-          if (m == -INFINITY) continue;
-          const float sc = exp2_approx(m - mx);
-          sum = fmaf(ld_cluster_f32(map_shared_to_rank(cta_l + h, rk)), sc, sum);
-          const float4 v = ld_cluster_f32x4(map_shared_to_rank(cta_o + h * kHeadDim + d0, rk));
-          o0 = fmaf(v.x, sc, o0);
-          o1 = fmaf(v.y, sc, o1);
-          o2 = fmaf(v.z, sc, o2);
-          o3 = fmaf(v.w, sc, o3);
+#pragma unroll
+        for (int rk = 0; rk < kMaxClusterSplits; ++rk) {
+          if (mr[rk] == -INFINITY) continue;
+          const float sc = exp2_approx(mr[rk] - mx);
+          sum = fmaf(lr[rk], sc, sum);
+          o0 = fmaf(vr[rk].x, sc, o0);
+          o1 = fmaf(vr[rk].y, sc, o1);
+          o2 = fmaf(vr[rk].z, sc, o2);
+          o3 = fmaf(vr[rk].w, sc, o3);
         }
       }
       if (has_prefix) {

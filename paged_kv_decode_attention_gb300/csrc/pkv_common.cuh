@@ -220,6 +220,11 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
   return v;
 }
 
+// Hint: bring the 128-byte line holding `p` into this SM's L1.
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 // ---- programmatic dependent launch ----
 // Wait until the grids this one depends on have completed and their writes
 // are visible (a no-op when the launch had no programmatic dependency).
