@@ -55,7 +55,7 @@ typedef enum pkv_status {
   PKV_OK = 0,
   PKV_ERR_NULL = 1,        /* a required pointer is NULL                       */
   PKV_ERR_SHAPE = 2,       /* a size is negative or inconsistent               */
-  PKV_ERR_UNSUPPORTED = 3, /* a shape this build has no kernel for             */
+  PKV_ERR_UNSUPPORTED = 3, /* a shape the library has no kernel for           */
   PKV_ERR_WORKSPACE = 4,   /* split-KV workspace missing or too small          */
   PKV_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute)   */
   PKV_ERR_EXHAUSTED = 6    /* a block pool has too few free blocks             */
