@@ -668,3 +668,37 @@ def test_fused_q8_short_chat_full_size():
         ref = oracle.paged_attention_f64(w.q[r:r + 1], oracle.dequantize_q8_0(kq_ref), oracle.dequantize_q8_0(vq_ref),
                                          np.arange(n, dtype=np.int32)[None, :], w.context_lens[r:r + 1], 1, w.scale)
         assert_close(got[r:r + 1], ref, what=f"full-size fused q8_0 request {r} vs oracle")
+
+
+# contexts that fill the whole block table (the new token in its last slot) or
+# stop one token short of it or one past a block, beside a short row and a
+# padding row; 41 blocks per table leave a ragged last tile in every format
+FULL_TABLE_BLOCKS = 41
+FULL_TABLE_CTX = [41 * 16, 41 * 16, 41 * 16 - 1, 40 * 16 + 1, 17, 0]
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8_0", "fp8_e4m3"])
+@pytest.mark.parametrize("bps", [0, 8, 1000])
+def test_contexts_that_fill_the_block_table(fmt, bps):
+    ctx = np.asarray(FULL_TABLE_CTX)
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("full-table", ctx, need + 12, seed=91, max_blocks=FULL_TABLE_BLOCKS)
+    assert w.max_blocks_per_seq == FULL_TABLE_BLOCKS
+    what = f"full table {fmt} bps={bps}"
+    if fmt == "bf16":
+        res = _both(w, bps)
+        _assert_same(res, what)
+        out, kf, vf = res[0]
+        kc, vc = w.k_cache.copy(), w.v_cache.copy()
+        oracle.kv_append(kc, vc, w.slot_mapping, w.k_new, w.v_new)
+        assert np.array_equal(kf.cpu().view(torch.int16).numpy().view(np.uint16), kc), f"{what}: K pool"
+        assert np.array_equal(vf.cpu().view(torch.int16).numpy().view(np.uint16), vc), f"{what}: V pool"
+        assert_close(bf16_to_f64(out), oracle.run_workload(w), what=f"{what} vs oracle")
+    elif fmt == "q8_0":
+        res, host = _q8_both(w, bps)
+        _assert_q8(res, host, w, what)
+    else:
+        res = _fp8_both(w, bps)
+        _assert_same_fp8(res, what)
+        _assert_fp8_oracle(res, w, what)
+    assert not res[0][0][ctx == 0].float().abs().sum()
