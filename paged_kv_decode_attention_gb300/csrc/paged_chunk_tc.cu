@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 template <bool kSplit>
 cudaError_t launch_chunk_variant(const CUtensorMap& kmap, const CUtensorMap& vmap, const ChunkArgs& a, dim3 grid,
                                  cudaStream_t stream) {
-  static bool done[64];
+  static std::atomic<bool> done[64];  // per device; host threads may race on a first call
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -654,7 +654,7 @@ constexpr int kStages = PKV_DECODE_STAGES;
 // device (function attributes are per device context).
 template <SplitMode kMode>
 cudaError_t allow_smem(int bytes) {
-  static bool done[64];
+  static std::atomic<bool> done[64];  // per device; host threads may race on a first call
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

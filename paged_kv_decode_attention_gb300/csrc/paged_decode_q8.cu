@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(kFused ? kQ8ThreadsFused : kQ8Threads, 1)
 
 template <bool kFused>
 cudaError_t allow_smem_q8() {
-  static bool done[64];
+  static std::atomic<bool> done[64];  // per device; host threads may race on a first call
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

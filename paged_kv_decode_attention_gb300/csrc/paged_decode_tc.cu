@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
 }
 
 cudaError_t allow_smem_dt() {
-  static bool done[64];
+  static std::atomic<bool> done[64];  // per device; host threads may race on a first call
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

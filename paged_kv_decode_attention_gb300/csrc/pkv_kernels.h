@@ -2,6 +2,7 @@
 // The exported C ABI (pkv_api.cu) validates arguments and calls these.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
