@@ -702,3 +702,22 @@ def test_contexts_that_fill_the_block_table(fmt, bps):
         _assert_same_fp8(res, what)
         _assert_fp8_oracle(res, w, what)
     assert not res[0][0][ctx == 0].float().abs().sum()
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "fp8_e4m3"])
+def test_fused_quantised_many_units_per_cta(fmt):
+    """130 requests x 8 KV heads = 1040 units with a new token over at most
+    152 persistent CTAs: every CTA handles 6 or more, so the q8_0 append
+    warp's 4-slot ready ring wraps and the E4M3 kernel's per-unit (parity)
+    buffers are reused many times."""
+    rng = np.random.default_rng(95)
+    ctx = rng.integers(1, 300, size=130)
+    need = int(sum(-(-int(c) // 16) for c in ctx))
+    w = W.build("many-units-" + fmt, ctx, need + 16, seed=96)
+    if fmt == "q8_0":
+        res, host = _q8_both(w, 1000)
+        _assert_q8(res, host, w, "q8_0 many units per CTA")
+    else:
+        res = _fp8_both(w, 1000)
+        _assert_same_fp8(res, "E4M3 many units per CTA")
+        _assert_fp8_oracle(res, w, "E4M3 many units per CTA")
